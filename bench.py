@@ -1,0 +1,474 @@
+"""Benchmark of the LatentIndex decode indexer step on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step = one decode step of the whole hot path for a 4-layer group over a
+batch of sequences: absorb the queries into the decoders (eq. 6), score the
+shared latent cache for all 4 layers in one pass (eq. 8), and take each
+layer's top-k.  The default workload is the batched 32K-context decode with
+an fp8 latent cache (32 sequences x 32,768 tokens, H=64, d=128, r=192,
+k=2048).  In the same run the bench also times, on the same batch, the
+hierarchical-selection variant (HS) and four native per-layer DSA indexer
+scans with their top-k (the baseline LatentIndex replaces), and reports them
+under "hs" and "native_x4".
+
+Timing: W warm-up steps, then K timed steps; before every step a 256 MiB
+buffer is written to flush the L2 (126 MB), outside the timed events; each
+step is bracketed by CUDA events on the launching stream and the per-step
+device times are summed; the max over ranks is taken.  `value` is the
+algorithmic HBM bytes of the step (latent + scales + queries + decoders +
+head weights + selected indices) per second.  `e2e` measures the same step
+through the C ABI with host buffers: the step's new queries and head weights
+are copied from pinned host memory and the selected indices copied back
+inside the timed region (the latent cache is device-resident state).
+
+With --impl reference the CPU oracle (fp64) is timed instead on a bounded
+sample of the same workload.  Under torchrun each rank runs its own batch
+(weak scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode indexer latency & HBM GB/s per 4-layer group at 8K-128K ctx"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="fp8_32k_b32")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-side", action="store_true", help="skip the HS / native side timings")
+    ap.add_argument("--cpu-sample-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0,
+            "source": "fallback"}
+
+
+def step_bytes(w) -> dict:
+    """Algorithmic bytes of one decode step (each tensor touched once)."""
+    esz = {"f32": 4, "bf16": 2, "fp8": 1}[w.lat_dtype]
+    qsz = {"f32": 4, "bf16": 2}[w.q_dtype]
+    toks = w.B * w.L
+    b = {
+        "latent": toks * w.r * esz,
+        "lat_scale": toks * 4 if w.lat_dtype == "fp8" else 0,
+        "q": w.B * w.T * w.G * w.H * w.d * qsz,
+        "D": w.G * w.r * w.d * qsz,
+        "w": w.B * w.T * w.G * w.H * 4,
+        "idx": w.B * w.T * w.G * w.k * 4,
+    }
+    b["total"] = sum(b.values())
+    return b
+
+
+def source_hash(paths) -> str:
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str):
+    """Per-launch DRAM bytes of the scan kernel from the committed ncu summary,
+    if it was taken on the current kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(workload)
+    if not e or e.get("source_hash") != source_hash(e.get("sources", [])):
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# --------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        import tempfile
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(float(r[3]) for r in rows
+                                                        if r[3].replace(".", "").isdigit()) if rows else None}
+
+
+# ------------------------------------------------------------------ reference
+
+def cpu_oracle_rate(w, seed: int, budget_s: float):
+    """Time the fp64 CPU oracle (absorb + score + TopK) on whole sequences of the
+    workload until about `budget_s` seconds of work; returns the line's fields."""
+    import numpy as np  # noqa: F401
+    import torch
+
+    import li_inputs
+    import oracle
+
+    oracle.build()
+    cores = oracle.default_threads()
+    per_seq = step_bytes(li_inputs.spec(w.name, B=1))["total"]
+    T_sample = w.T if w.T == 1 else 1
+    done, elapsed, seqs = 0, 0.0, 0
+    bytes_done = 0
+    while (seqs == 0 or elapsed < budget_s) and seqs < w.B:
+        one = li_inputs.spec(w.name, B=1, T=T_sample, native=False,
+                             pos0=(w.pos0 + w.T - 1) if w.pos0 >= 0 else -1)
+        x = li_inputs.make_workload(one, seed=seed + 1000 + seqs)
+        t0 = time.perf_counter()
+        qabs = oracle.absorb(x["q"], x["D"])
+        u = oracle.score(x["latent"], x["lat_scale"], qabs, x["w"], q_pos=x["q_pos"])
+        vl = None
+        if x["q_pos"] is not None:
+            vl = np.full(one.G, int(x["q_pos"][0]) + 1, dtype=np.int32)
+        oracle.topk(u.reshape(-1, one.L), one.k, valid_len=vl)
+        elapsed += time.perf_counter() - t0
+        seqs += 1
+        bytes_done += step_bytes(one)["total"]
+        del x, qabs, u
+        torch.cuda.empty_cache() if torch.cuda.is_available() else None
+    gbs = bytes_done / elapsed / 1e9
+    sample = (f"{seqs} of {w.B} sequences of {w.name}" if w.T == 1 else
+              f"{seqs} query (last position) of {w.T} of {w.name}")
+    return {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": sample + f", fp64, {elapsed:.1f} s", "seconds": elapsed,
+            "bytes": bytes_done, "per_sequence_bytes": per_seq}
+
+
+def run_reference(a, w):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    t0 = time.perf_counter()
+    steps = []
+    for i in range(max(1, a.steps if a.steps <= 3 else 1)):
+        steps.append(cpu_oracle_rate(w, a.seed + i, a.cpu_sample_seconds))
+    cb = steps[-1]
+    sb = step_bytes(w)["total"]
+    ms = sb / (cb["value"] * 1e9) * 1e3
+    line = {
+        "impl": "reference", "metric": METRIC, "value": cb["value"], "unit": "GB/s",
+        "n_gpus": a.gpus, "steps": len(steps), "warmup": 0, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": w.name, "B": w.B, "L": w.L, "G": w.G, "H": w.H,
+                                        "d": w.d, "r": w.r, "k": w.k, "T": w.T},
+        "cpu_baseline": {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")},
+        "e2e": {"value": cb["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "wall_s": time.perf_counter() - t0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------------ ours
+
+def run_ours(a, w):
+    import torch
+
+    import li_inputs
+    import shared_latent_key_cache_b300 as li
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    x = li_inputs.make_workload(li_inputs.spec(w.name, native=not a.no_side and w.T == 1),
+                                seed=a.seed + rank, device=dev)
+    absd = {"f32": "f32", "bf16": "bf16", "fp8": "fp8"}[w.lat_dtype]
+    stream = torch.cuda.current_stream(dev)
+    B, T, G, H, r, L, k = w.B, w.T, w.G, w.H, w.r, w.L, w.k
+
+    q_abs = torch.empty(B, T, G, H, r, dtype={"f32": torch.float32, "bf16": torch.bfloat16,
+                                              "fp8": torch.uint8}[absd], device=dev)
+    q_scale = torch.empty(B, T, G, H, dtype=torch.float32, device=dev) if absd == "fp8" else None
+    scores = torch.empty(B, T, G, L, dtype=torch.float32, device=dev)
+    idx = torch.empty(B, T, G, k, dtype=torch.int32, device=dev)
+    vl = None
+    if x["q_pos"] is not None:
+        vl = (x["q_pos"] + 1).repeat_interleave(G).contiguous()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def chk(st, what):
+        if st != 0:
+            raise RuntimeError(f"{what}: {li.li_status_string(st)}")
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        chk(li.li_absorb_queries(x["q"], x["D"], q_abs, q_scale, stream), "absorb")
+        if ev is not None:
+            ev[1].record(stream)
+        chk(li.li_score_group(x["latent"], x["lat_scale"], q_abs, q_scale, x["w"], scores,
+                              q_pos=x["q_pos"], stream=stream), "score")
+        if ev is not None:
+            ev[2].record(stream)
+        chk(li.li_topk(scores, k, idx, None, vl, stream), "topk")
+        if ev is not None:
+            ev[3].record(stream)
+
+    for _ in range(a.warmup):
+        flush.fill_(1)
+        step()
+    st = li.li_device_status(stream)
+    if st != 0:
+        raise RuntimeError(li.li_status_string(st))
+
+    K = a.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    barrier = (lambda: torch.distributed.barrier()) if ws > 1 else (lambda: None)
+    barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        t_wall = time.perf_counter()
+        for i in range(K):
+            flush.fill_(i & 0xFF)
+            step(evs[i])
+        torch.cuda.synchronize(dev)
+        t_wall = time.perf_counter() - t_wall
+    barrier()
+    st = li.li_device_status(stream)
+    if st != 0:
+        raise RuntimeError(li.li_status_string(st))
+    per = [[e[j].elapsed_time(e[j + 1]) for j in range(3)] for e in evs]
+    step_ms = sum(p[0] + p[1] + p[2] for p in per)
+    tot = torch.tensor([step_ms], device=dev, dtype=torch.float64)
+    if ws > 1:
+        torch.distributed.all_reduce(tot, op=torch.distributed.ReduceOp.MAX)
+    ms_per_step = float(tot.item()) / K
+    sb = step_bytes(w)
+    value = sb["total"] * ws / (ms_per_step * 1e-3) / 1e9
+    absorb_us = statistics.median(p[0] for p in per) * 1e3
+    score_us = statistics.mean(p[1] for p in per) * 1e3
+    topk_us = statistics.median(p[2] for p in per) * 1e3
+    clocks = clk.summary()
+
+    # ---- e2e: the same step through the C ABI with host buffers
+    q_h = x["q"].cpu().pin_memory()
+    w_h = x["w"].cpu().pin_memory()
+    idx_h = torch.empty(idx.shape, dtype=torch.int32).pin_memory()
+    q_d = torch.empty_like(x["q"])
+    w_d = torch.empty_like(x["w"])
+    E = min(K, 500)
+    e0 = [torch.cuda.Event(enable_timing=True) for _ in range(E)]
+    e1 = [torch.cuda.Event(enable_timing=True) for _ in range(E)]
+    for i in range(E):
+        flush.fill_(i & 0xFF)
+        e0[i].record(stream)
+        q_d.copy_(q_h, non_blocking=True)
+        w_d.copy_(w_h, non_blocking=True)
+        chk(li.li_absorb_queries(q_d, x["D"], q_abs, q_scale, stream), "absorb")
+        chk(li.li_score_group(x["latent"], x["lat_scale"], q_abs, q_scale, w_d, scores,
+                              q_pos=x["q_pos"], stream=stream), "score")
+        chk(li.li_topk(scores, k, idx, None, vl, stream), "topk")
+        idx_h.copy_(idx, non_blocking=True)
+        e1[i].record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = sum(e0[i].elapsed_time(e1[i]) for i in range(E)) / E
+    e2e_t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+    if ws > 1:
+        torch.distributed.all_reduce(e2e_t, op=torch.distributed.ReduceOp.MAX)
+    e2e_ms = float(e2e_t.item())
+    h2d = q_h.numel() * q_h.element_size() + w_h.numel() * w_h.element_size()
+    d2h = idx_h.numel() * idx_h.element_size()
+
+    # ---- side timings on the same batch: HS, and 4 native per-layer scans + top-k
+    side = {}
+    if not a.no_side and T == 1:
+        side = side_timings(a, w, x, q_abs, q_scale, li, stream, flush, dev)
+
+    # ---- roofline of the dominant kernel (the group scan)
+    pk = peaks()
+    esz = {"f32": 4, "bf16": 2, "fp8": 1}[w.lat_dtype]
+    scan_bytes = (B * L * (r * esz + (4 if w.lat_dtype == "fp8" else 0)) +
+                  q_abs.numel() * q_abs.element_size() + x["w"].numel() * 4)
+    achieved = scan_bytes / (score_us * 1e-6) / 1e9
+    tr = ncu_traffic(w.name)
+    roof = {"kernel": "score_tc_kernel (group scan)", "bound": "hbm", "achieved": achieved,
+            "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
+            "traffic": tr, "peak_source": pk["source"] + " copy bandwidth",
+            "algorithmic_bytes_per_launch": scan_bytes,
+            "flops_per_launch": 2 * B * T * L * G * H * r}
+
+    if rank == 0:
+        cb = None
+        if ws == 1:
+            cb = cpu_oracle_rate(w, a.seed, a.cpu_sample_seconds)
+            cb = {k2: cb[k2] for k2 in ("value", "unit", "cores", "kind", "sample")}
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": K,
+            "warmup": a.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": w.lat_dtype, "data": "synthetic",
+            "config": {"workload": w.name, "B": B, "T": T, "L": L, "G": G, "H": H, "d": w.d, "r": r,
+                       "k": k, "latent": {"fp8": "fp8 e4m3 + fp32 per-token scale", "bf16": "bf16",
+                                          "f32": "fp32"}[w.lat_dtype],
+                       "step": "absorb + 4-layer group score + per-layer top-k",
+                       "l2": "flushed (256 MiB write) before every step, outside the timed events",
+                       "parallelism": f"replicas{ws}" if ws > 1 else "single GPU"},
+            "latency_us": ms_per_step * 1e3,
+            "tokens_scored_per_s": B * T * G * L * ws / (ms_per_step * 1e-3),
+            "kernels_us": {"absorb": absorb_us, "score": score_us, "topk": topk_us},
+            "step_bytes": sb,
+            "wall_s_timed": t_wall,
+            "e2e": {"value": sb["total"] * ws / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                    "resident": "latent cache and decoders (device state across decode steps)"},
+            "gpu_launches": 3 * K,
+            "roofline": roof,
+            "clocks": clocks,
+            "cpu_baseline": cb,
+        }
+        line.update(side)
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+def side_timings(a, w, x, q_abs, q_scale, li, stream, flush, dev):
+    import torch
+    B, G, H, r, L, k, d = w.B, w.G, w.H, w.r, w.L, w.k, w.d
+    out = {}
+    reps = max(5, min(200, a.steps // 10))
+
+    def timeit(fn):
+        for _ in range(3):
+            flush.fill_(0)
+            fn()
+        ts = []
+        for i in range(reps):
+            flush.fill_(i & 0xFF)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            ts.append((e0, e1))
+        torch.cuda.synchronize(dev)
+        return statistics.median(e0.elapsed_time(e1) for e0, e1 in ts) * 1e3
+
+    m = w.m if w.m else 8192
+    if m <= L:
+        cand = torch.empty(B, m, dtype=torch.int32, device=dev)
+        hidx = torch.empty(B, G, k, dtype=torch.int32, device=dev)
+        wsb = torch.empty(li.li_hs_workspace_size(B, G, L, m, k), dtype=torch.uint8, device=dev)
+
+        def hs():
+            st = li.li_absorb_queries(x["q"], x["D"], q_abs, q_scale, stream)
+            st |= li.li_hs_select(x["latent"], x["lat_scale"], q_abs, q_scale, x["w"], m, k, cand,
+                                  hidx, wsb, None, stream)
+            assert st == 0
+        hs_us = timeit(hs)
+        out["hs"] = {"m": m, "latency_us": hs_us,
+                     "scored_positions_per_seq": L + (G - 1) * min(m, L)}
+
+    if "keys" in x:
+        q8 = torch.empty(B, 1, 1, H, d, dtype=torch.uint8, device=dev)
+        qs8 = torch.empty(B, 1, 1, H, dtype=torch.float32, device=dev)
+        qls = [x["q"][:, :, l:l + 1].contiguous() for l in range(G)]
+        wls = [x["w"][:, 0, l].contiguous() for l in range(G)]
+        ns = torch.empty(B, L, dtype=torch.float32, device=dev)
+        nidx = torch.empty(B, k, dtype=torch.int32, device=dev)
+
+        def native(with_topk=True):
+            for l in range(G):
+                st = li.li_absorb_queries(qls[l], None, q8, qs8, stream)
+                st |= li.li_native_score(x["keys"][l], x["key_scale"][l], q8.view(B, H, d),
+                                         qs8.view(B, H), wls[l], ns, stream)
+                if with_topk:
+                    st |= li.li_topk(ns, k, nidx, None, None, stream)
+                assert st == 0
+        n_us = timeit(lambda: native(True))
+        n_scan_us = timeit(lambda: native(False))
+        nbytes = G * B * L * (d + 4)
+        out["native_x4"] = {"latency_us": n_us, "scan_only_us": n_scan_us,
+                            "cache_bytes": nbytes, "scan_gbs": nbytes / (n_scan_us * 1e-6) / 1e9}
+    return out
+
+
+def main():
+    a = parse()
+    import li_inputs
+    w = li_inputs.spec(a.workload)
+    if a.impl == "reference":
+        run_reference(a, w)
+    else:
+        run_ours(a, w)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,181 @@
+/*
+ * li.h -- C ABI of libli_b300.so: the LatentIndex decode/prefill indexer scan
+ * over a shared latent cache, for NVIDIA B300 (sm_103a).
+ *
+ * What the library computes (sources: "LatentIndex: Cross-Layer Sharing with
+ * Layer-Specific Selection for Sparse Attention", summary page, Methodology,
+ * eqs. (6)-(8) and the "Hierarchical Selection" paragraph; "LatentIndex --
+ * Shared indexer cache, per-layer token choice", explainer page):
+ *
+ *   a group of G consecutive layers caches ONE latent c_t (r values) per
+ *   token; layer l folds its decoder D_l (stored r x d) into each indexer-head
+ *   query, q~_{l,h} = D_l q_{l,h}                                   (eq. 6)
+ *   and scores every valid cached token with
+ *   u_l(t) = sum_h w_{l,h} ReLU(q~_{l,h} . c_t + beta_{l,h})       (eq. 8)
+ *   then keeps its own top-k token set.  Hierarchical selection (HS) lets the
+ *   group's first layer (the anchor) propose its top-m candidates and the
+ *   other layers (followers) rescore and select only inside them.
+ *
+ * Conventions (all entry points):
+ *  - Pointers named as tensors are DEVICE pointers owned by the caller; the
+ *    library never allocates device memory.  Tensors are dense, row-major, in
+ *    the layout written next to each argument, with 16-byte aligned base
+ *    addresses.  A NULL optional pointer means "absent" as documented.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every
+ *    call is asynchronous on that stream; its return value covers argument
+ *    validation and launch errors only.  Errors a kernel detects on the device
+ *    (a bounded wait that ran out) are latched in a per-device status word and
+ *    read with li_device_status().
+ *  - Argument errors are reported before any CUDA call is made.
+ *  - Storage types: LI_F32 float, LI_BF16 bfloat16, LI_FP8_E4M3 OCP FP8 E4M3
+ *    ("fn") codes with one fp32 scale per row: value = scale * decode(code).
+ *    Scales must be >= 0 and finite.
+ *  - Calls are reentrant; concurrent calls on different streams are safe.
+ */
+#ifndef LI_B300_H
+#define LI_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { LI_F32 = 0, LI_BF16 = 1, LI_FP8_E4M3 = 2 } li_dtype;
+
+enum {
+    LI_OK = 0,
+    LI_ERR_INVALID_ARG = -1,   /* NULL required pointer, non-positive size, bad enum */
+    LI_ERR_ALIGNMENT = -2,     /* a tensor base address is not 16-byte aligned        */
+    LI_ERR_UNSUPPORTED = -3,   /* valid arguments outside what the kernels implement */
+    LI_ERR_WORKSPACE = -4,     /* workspace missing or smaller than required         */
+    LI_ERR_CUDA = -5,          /* a CUDA runtime/driver call or a launch failed      */
+    LI_ERR_TIMEOUT = -6,       /* device: a bounded wait inside a kernel ran out     */
+    LI_ERR_DEVICE_BOUNDS = -7  /* device: an index outside its tensor was skipped    */
+};
+
+/* Library version, major*10000 + minor*100 + patch. */
+int li_version(void);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *li_status_string(int status);
+
+/*
+ * Query-side decoder absorption (summary page, eq. (6); explainer page:
+ * q.(D c) = (D^T q).c lets the decoder act once on the query instead of on
+ * every cached latent).
+ *
+ *   q      [B][T][G][H][d]  q_t in {LI_F32, LI_BF16}
+ *   D      [G][r][d]        D_t in {LI_F32, LI_BF16}; NULL = identity
+ *                           (requires r == d: rows of q are only converted /
+ *                           quantised, which prepares native DSA queries)
+ *   q_abs  [B][T][G][H][r]  out, abs_t in {LI_F32, LI_BF16, LI_FP8_E4M3}
+ *   q_abs_scale [B][T][G][H] out fp32: required iff abs_t == LI_FP8_E4M3
+ *                           (per-row scale = max|row| / 448), else ignored.
+ * Accumulation is fp32; the result is rounded once to abs_t.
+ * Limits: 1 <= d <= 1024, 1 <= r <= 256.
+ */
+int li_absorb_queries(const void *q, int q_t, const void *D, int D_t,
+                      int B, int T, int G, int H, int d, int r,
+                      void *q_abs, int abs_t, float *q_abs_scale, void *stream);
+
+/*
+ * Group scoring on the shared latent cache (summary page, eq. (8)), all G
+ * layers of the group in one pass over the cache.
+ *
+ *   latent      [B][L][r]     lat_t; LI_FP8_E4M3 needs lat_scale [B][L];
+ *                             lat_scale is optional (NULL = 1) otherwise
+ *   q_abs       [B][T][G][H][r] abs_t, q_abs_scale [B][T][G][H] as produced
+ *                             by li_absorb_queries (NULL = 1 unless fp8)
+ *   w           [B][T][G][H]  fp32 head weights (query dependent)
+ *   beta        [B][T][G][H]  fp32 or NULL (= 0): beta = q^N . b of eq. (6)
+ *   q_pos       [T] int32 or NULL.  NULL: every cached token is valid (decode).
+ *                             Otherwise query t sees tokens s <= q_pos[t]
+ *                             (causal prefill); q_pos[t] >= 0.
+ *   scores      [B][T][G][L]  fp32 out: u_l(t) for valid t.  Entries past a
+ *                             query's causal limit are not written.
+ * Supported dtype pairs: (F32, F32) on CUDA cores; (BF16, BF16) and
+ * (FP8_E4M3, FP8_E4M3) on the tensor cores (tcgen05) when r % 64 == 0,
+ * r <= 256, H in {16, 32, 64, 128} and G*H <= 256; any other pair or shape
+ * runs on CUDA cores when G*H*r <= 8192 and r <= 256, else LI_ERR_UNSUPPORTED.
+ */
+int li_score_group(const void *latent, int lat_t, const float *lat_scale,
+                   const void *q_abs, int abs_t, const float *q_abs_scale,
+                   const float *w, const float *beta, const int32_t *q_pos,
+                   int B, int T, int G, int H, int r, int L,
+                   float *scores, void *stream);
+
+/*
+ * Per-row top-k (summary page, TopK after eq. (8)): for each of `rows` score
+ * rows of length L, the indices of the min(k, V) largest scores over the
+ * valid prefix [0, V), V = valid_len[row] (NULL: V = L; values are clamped to
+ * [0, L]).  Exact: a radix select on order-preserving 32-bit keys.  Among
+ * equal scores at the threshold the lower index is taken.  NaN scores are
+ * not allowed.
+ *
+ *   scores [rows][L] fp32; idx [rows][k] int32 out (set in unspecified order,
+ *   slots past min(k, V) hold -1); vals [rows][k] fp32 out or NULL (the score
+ *   of each selected index, -inf in padded slots).
+ * Limits: 1 <= k <= 65536, L < 2^31.
+ */
+int li_topk(const float *scores, int64_t rows, int L, const int32_t *valid_len, int k,
+            int32_t *idx, float *vals, void *stream);
+
+/* Workspace bytes li_hs_select needs for these sizes. */
+size_t li_hs_workspace_size(int B, int G, int L, int m, int k);
+
+/*
+ * Hierarchical selection for one decode step of B sequences (summary page,
+ * "Hierarchical Selection"; explainer page: the anchor fills a cart of
+ * candidates and each follower picks its own top-k from the cart only).
+ *
+ * The anchor (layer 0 of the group) scores all L cached tokens and keeps its
+ * top-m positions as the candidate set C_b (m >= k) and its top-k as its own
+ * selection; every follower l = 1..G-1 rescores only the min(m, L) candidate
+ * rows of the latent and keeps its top-k inside C_b.  Scored positions per
+ * sequence: L + (G-1) min(m, L).
+ *
+ *   latent, lat_t, lat_scale, q_abs (T = 1), abs_t, q_abs_scale, w, beta
+ *                    as for li_score_group with T = 1
+ *   cand [B][m] int32 out: anchor candidates (-1 padded when L < m)
+ *   idx  [B][G][k] int32 out: per-layer selections (-1 padded)
+ *   ws   device workspace of at least li_hs_workspace_size(B, G, L, m, k)
+ *        bytes, 256-byte aligned.
+ */
+int li_hs_select(const void *latent, int lat_t, const float *lat_scale,
+                 const void *q_abs, int abs_t, const float *q_abs_scale,
+                 const float *w, const float *beta,
+                 int B, int G, int H, int r, int L, int m, int k,
+                 int32_t *cand, int32_t *idx, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * Native per-layer DSA lightning indexer over one layer's own key cache, the
+ * baseline LatentIndex replaces (explainer page: "DSA lightning indexer",
+ * "Indexer key cache" of 132 B per token per layer = 128 fp8 values + one
+ * fp32 scale):  I_t = sum_h w_h ReLU(q_h . k_t).
+ *
+ *   keys  [B][L][d]  key_t (LI_FP8_E4M3 with key_scale [B][L], or LI_BF16)
+ *   q     [B][H][d]  q_t matching key_t (fp8 rows need q_scale [B][H]; use
+ *                    li_absorb_queries with D = NULL to prepare them)
+ *   w     [B][H]     fp32
+ *   scores [B][L]    fp32 out
+ * Same kernels and limits as li_score_group with G = 1, T = 1, r = d.
+ */
+int li_native_score(const void *keys, int key_t, const float *key_scale,
+                    const void *q, int q_t, const float *q_scale, const float *w,
+                    int B, int H, int d, int L, float *scores, void *stream);
+
+/*
+ * Synchronises `stream`, then returns and clears the calling device's status
+ * word: LI_OK, or the first device-side error latched since the last call
+ * (LI_ERR_TIMEOUT, LI_ERR_DEVICE_BOUNDS), or LI_ERR_CUDA if the
+ * synchronisation itself failed.
+ */
+int li_device_status(void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LI_B300_H */

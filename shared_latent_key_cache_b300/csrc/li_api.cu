@@ -1,0 +1,376 @@
+// li_api.cu -- the C ABI of libli_b300.so (declared in include/li.h).
+//
+// Each entry point validates its arguments on the host (returning a status
+// before any CUDA call when they are wrong), picks the kernel for the dtype
+// pair and shape, and launches asynchronously on the caller's stream.  The
+// library owns no device memory except one status word per device, where
+// kernels latch device-side errors (a bounded wait that ran out, an index
+// outside its tensor); li_device_status() reads and clears it.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+
+#include "li_internal.cuh"
+
+namespace li {
+
+__device__ int g_li_status;
+
+int *device_status_ptr()
+{
+    constexpr int kMaxDev = 64;
+    static std::atomic<int *> cache[kMaxDev];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev)
+        return nullptr;
+    int *p = cache[dev].load(std::memory_order_acquire);
+    if (p == nullptr) {
+        void *addr = nullptr;
+        if (cudaGetSymbolAddress(&addr, g_li_status) != cudaSuccess)
+            return nullptr;
+        p = static_cast<int *>(addr);
+        cache[dev].store(p, std::memory_order_release);
+    }
+    return p;
+}
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool valid_dtype(int t) { return t == LI_F32 || t == LI_BF16 || t == LI_FP8_E4M3; }
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? LI_OK : LI_ERR_CUDA; }
+
+// Shared memory the CUDA-core scorer needs for this shape.
+size_t simt_smem(int Gs, int H, int r)
+{
+    const size_t N = static_cast<size_t>(Gs) * H;
+    return sizeof(float) * (N * r + 2 * N + 128 * (static_cast<size_t>(r) + 1));
+}
+
+// Validates the scoring arguments shared by li_score_group / li_native_score /
+// li_hs_select.  Returns LI_OK or an error status.
+int check_score_args(const void *latent, int lat_t, const float *lat_scale, const void *q_abs,
+                     int abs_t, const float *q_abs_scale, const float *w, const float *beta,
+                     const int32_t *q_pos, const void *out, int B, int T, int G, int H, int r, int L)
+{
+    if (!latent || !q_abs || !w || !out)
+        return LI_ERR_INVALID_ARG;
+    if (!valid_dtype(lat_t) || !valid_dtype(abs_t))
+        return LI_ERR_INVALID_ARG;
+    if (B <= 0 || T <= 0 || G <= 0 || H <= 0 || r <= 0 || L <= 0)
+        return LI_ERR_INVALID_ARG;
+    if (lat_t == LI_FP8_E4M3 && !lat_scale)
+        return LI_ERR_INVALID_ARG;
+    if (abs_t == LI_FP8_E4M3 && !q_abs_scale)
+        return LI_ERR_INVALID_ARG;
+    if (!aligned16(latent) || !aligned16(q_abs) || !aligned16(w) || !aligned16(out) ||
+        !aligned16(lat_scale) || !aligned16(q_abs_scale) || !aligned16(beta) || !aligned16(q_pos))
+        return LI_ERR_ALIGNMENT;
+    if (r > 256)
+        return LI_ERR_UNSUPPORTED;
+    return LI_OK;
+}
+
+int run_score(const ScoreParams &p, cudaStream_t s)
+{
+    if (score_tc_supported(p))
+        return cuda_status(launch_score_tc(p, s));
+    if (simt_smem(p.Gs, p.H, p.r) <= 227 * 1024)
+        return cuda_status(launch_score_simt(p, s));
+    return LI_ERR_UNSUPPORTED;
+}
+
+bool score_supported(const ScoreParams &p)
+{
+    return score_tc_supported(p) || simt_smem(p.Gs, p.H, p.r) <= 227 * 1024;
+}
+
+} // namespace
+} // namespace li
+
+using namespace li;
+
+extern "C" {
+
+int li_version(void) { return 100; }
+
+const char *li_status_string(int status)
+{
+    switch (status) {
+    case LI_OK: return "LI_OK";
+    case LI_ERR_INVALID_ARG: return "LI_ERR_INVALID_ARG: invalid argument";
+    case LI_ERR_ALIGNMENT: return "LI_ERR_ALIGNMENT: tensor base address not 16-byte aligned";
+    case LI_ERR_UNSUPPORTED: return "LI_ERR_UNSUPPORTED: dtype pair or shape not implemented";
+    case LI_ERR_WORKSPACE: return "LI_ERR_WORKSPACE: workspace missing or too small";
+    case LI_ERR_CUDA: return "LI_ERR_CUDA: CUDA call or launch failed";
+    case LI_ERR_TIMEOUT: return "LI_ERR_TIMEOUT: a bounded wait inside a kernel ran out";
+    case LI_ERR_DEVICE_BOUNDS: return "LI_ERR_DEVICE_BOUNDS: an index outside its tensor was skipped";
+    default: return "unknown status";
+    }
+}
+
+int li_absorb_queries(const void *q, int q_t, const void *D, int D_t, int B, int T, int G, int H,
+                      int d, int r, void *q_abs, int abs_t, float *q_abs_scale, void *stream)
+{
+    if (!q || !q_abs)
+        return LI_ERR_INVALID_ARG;
+    if ((q_t != LI_F32 && q_t != LI_BF16) || !valid_dtype(abs_t))
+        return LI_ERR_INVALID_ARG;
+    if (D && D_t != LI_F32 && D_t != LI_BF16)
+        return LI_ERR_INVALID_ARG;
+    if (B <= 0 || T <= 0 || G <= 0 || H <= 0 || d <= 0 || r <= 0)
+        return LI_ERR_INVALID_ARG;
+    if (!D && r != d)
+        return LI_ERR_INVALID_ARG;
+    if (abs_t == LI_FP8_E4M3 && !q_abs_scale)
+        return LI_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(D) || !aligned16(q_abs) ||
+        (abs_t == LI_FP8_E4M3 && !aligned16(q_abs_scale)))
+        return LI_ERR_ALIGNMENT;
+    if (r > 256 || d > 1024 || G > 65535)
+        return LI_ERR_UNSUPPORTED;
+    const int64_t N = static_cast<int64_t>(B) * T;
+    if (N * H > 0x7FFFFFFFll * 64)
+        return LI_ERR_UNSUPPORTED;
+    AbsorbParams p;
+    p.q = q;
+    p.D = D;
+    p.q_abs = q_abs;
+    p.q_abs_scale = abs_t == LI_FP8_E4M3 ? q_abs_scale : nullptr;
+    p.q_t = q_t;
+    p.D_t = D ? D_t : LI_F32;
+    p.abs_t = abs_t;
+    p.N = static_cast<int>(N);
+    p.G = G;
+    p.H = H;
+    p.d = d;
+    p.r = r;
+    if (N > 0x7FFFFFFF)
+        return LI_ERR_UNSUPPORTED;
+    return cuda_status(launch_absorb(p, static_cast<cudaStream_t>(stream)));
+}
+
+int li_score_group(const void *latent, int lat_t, const float *lat_scale, const void *q_abs,
+                   int abs_t, const float *q_abs_scale, const float *w, const float *beta,
+                   const int32_t *q_pos, int B, int T, int G, int H, int r, int L, float *scores,
+                   void *stream)
+{
+    int st = check_score_args(latent, lat_t, lat_scale, q_abs, abs_t, q_abs_scale, w, beta, q_pos,
+                              scores, B, T, G, H, r, L);
+    if (st != LI_OK)
+        return st;
+    ScoreParams p{};
+    p.latent = latent;
+    p.lat_scale = lat_scale;
+    p.q_abs = q_abs;
+    p.q_abs_scale = q_abs_scale;
+    p.w = w;
+    p.beta = beta;
+    p.q_pos = q_pos;
+    p.gather_idx = nullptr;
+    p.scores = scores;
+    p.lat_t = lat_t;
+    p.abs_t = abs_t;
+    p.B = B;
+    p.T = T;
+    p.Gtot = G;
+    p.g0 = 0;
+    p.Gs = G;
+    p.H = H;
+    p.r = r;
+    p.L_lat = L;
+    p.L_out = L;
+    p.n_gather = 0;
+    if (!score_supported(p))
+        return LI_ERR_UNSUPPORTED;
+    p.status = device_status_ptr();
+    if (!p.status)
+        return LI_ERR_CUDA;
+    return run_score(p, static_cast<cudaStream_t>(stream));
+}
+
+int li_topk(const float *scores, int64_t rows, int L, const int32_t *valid_len, int k, int32_t *idx,
+            float *vals, void *stream)
+{
+    if (!scores || !idx)
+        return LI_ERR_INVALID_ARG;
+    if (rows < 0 || L < 0 || k <= 0 || k > (1 << 30))
+        return LI_ERR_INVALID_ARG;
+    if (!aligned16(scores) || !aligned16(idx) || !aligned16(vals) || !aligned16(valid_len))
+        return LI_ERR_ALIGNMENT;
+    if (rows == 0)
+        return LI_OK;
+    TopkParams p{};
+    p.scores = scores;
+    p.rows = rows;
+    p.in_stride = L;
+    p.L_row = L;
+    p.valid_len = valid_len;
+    p.k = k;
+    p.idx = idx;
+    p.vals = vals;
+    p.rows_per_group = 1;
+    p.group_stride = 1;
+    p.row_offset = 0;
+    p.map = nullptr;
+    p.map_stride = 0;
+    p.status = device_status_ptr();
+    if (!p.status)
+        return LI_ERR_CUDA;
+    return cuda_status(launch_topk(p, static_cast<cudaStream_t>(stream)));
+}
+
+size_t li_hs_workspace_size(int B, int G, int L, int m, int k)
+{
+    if (B <= 0 || G <= 0 || L <= 0 || m <= 0 || k <= 0)
+        return 0;
+    const size_t anchor = align256(sizeof(float) * static_cast<size_t>(B) * L);
+    const size_t cvals = align256(sizeof(float) * static_cast<size_t>(B) * m);
+    const size_t fol = align256(sizeof(float) * static_cast<size_t>(B) * (G - 1) * m);
+    return anchor + cvals + fol;
+}
+
+int li_hs_select(const void *latent, int lat_t, const float *lat_scale, const void *q_abs, int abs_t,
+                 const float *q_abs_scale, const float *w, const float *beta, int B, int G, int H,
+                 int r, int L, int m, int k, int32_t *cand, int32_t *idx, void *ws, size_t ws_bytes,
+                 void *stream)
+{
+    int st = check_score_args(latent, lat_t, lat_scale, q_abs, abs_t, q_abs_scale, w, beta, nullptr,
+                              cand, B, 1, G, H, r, L);
+    if (st != LI_OK)
+        return st;
+    if (!idx || m <= 0 || k <= 0 || m < k)
+        return LI_ERR_INVALID_ARG;
+    if (!aligned16(idx))
+        return LI_ERR_ALIGNMENT;
+    const size_t need = li_hs_workspace_size(B, G, L, m, k);
+    if (!ws || ws_bytes < need)
+        return LI_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
+        return LI_ERR_ALIGNMENT;
+
+    uint8_t *wsb = static_cast<uint8_t *>(ws);
+    float *anchor = reinterpret_cast<float *>(wsb);
+    float *cvals = reinterpret_cast<float *>(wsb + align256(sizeof(float) * static_cast<size_t>(B) * L));
+    float *fol = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(cvals) +
+                                           align256(sizeof(float) * static_cast<size_t>(B) * m));
+    const int nc = m < L ? m : L;
+
+    ScoreParams a{};
+    a.latent = latent;
+    a.lat_scale = lat_scale;
+    a.q_abs = q_abs;
+    a.q_abs_scale = q_abs_scale;
+    a.w = w;
+    a.beta = beta;
+    a.q_pos = nullptr;
+    a.gather_idx = nullptr;
+    a.scores = anchor;
+    a.lat_t = lat_t;
+    a.abs_t = abs_t;
+    a.B = B;
+    a.T = 1;
+    a.Gtot = G;
+    a.g0 = 0;
+    a.Gs = 1;
+    a.H = H;
+    a.r = r;
+    a.L_lat = L;
+    a.L_out = L;
+    a.n_gather = 0;
+    ScoreParams f = a;
+    f.gather_idx = cand;
+    f.scores = fol;
+    f.g0 = 1;
+    f.Gs = G - 1;
+    f.L_out = m;
+    f.n_gather = nc;
+    if (!score_supported(a) || (G > 1 && !score_supported(f)))
+        return LI_ERR_UNSUPPORTED;
+
+    int *status = device_status_ptr();
+    if (!status)
+        return LI_ERR_CUDA;
+    a.status = f.status = status;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    // 1. anchor scores over all L positions
+    st = run_score(a, s);
+    if (st != LI_OK)
+        return st;
+    // 2. anchor top-m -> candidate set (and its scores)
+    TopkParams t{};
+    t.scores = anchor;
+    t.rows = B;
+    t.in_stride = L;
+    t.L_row = L;
+    t.valid_len = nullptr;
+    t.k = m;
+    t.idx = cand;
+    t.vals = cvals;
+    t.rows_per_group = 1;
+    t.group_stride = 1;
+    t.row_offset = 0;
+    t.map = nullptr;
+    t.map_stride = 0;
+    t.status = status;
+    st = cuda_status(launch_topk(t, s));
+    if (st != LI_OK)
+        return st;
+    // 3. the anchor's own top-k, inside its candidates
+    TopkParams ta = t;
+    ta.scores = cvals;
+    ta.in_stride = m;
+    ta.L_row = nc;
+    ta.k = k;
+    ta.idx = idx;
+    ta.vals = nullptr;
+    ta.group_stride = G;
+    ta.map = cand;
+    ta.map_stride = m;
+    st = cuda_status(launch_topk(ta, s));
+    if (st != LI_OK || G == 1)
+        return st;
+    // 4. followers rescore the candidate rows of the latent
+    st = run_score(f, s);
+    if (st != LI_OK)
+        return st;
+    // 5. followers' top-k inside the candidates
+    TopkParams tf = ta;
+    tf.scores = fol;
+    tf.rows = static_cast<int64_t>(B) * (G - 1);
+    tf.rows_per_group = G - 1;
+    tf.group_stride = G;
+    tf.row_offset = 1;
+    return cuda_status(launch_topk(tf, s));
+}
+
+int li_native_score(const void *keys, int key_t, const float *key_scale, const void *q, int q_t,
+                    const float *q_scale, const float *w, int B, int H, int d, int L, float *scores,
+                    void *stream)
+{
+    return li_score_group(keys, key_t, key_scale, q, q_t, q_scale, w, nullptr, nullptr, B, 1, 1, H,
+                          d, L, scores, stream);
+}
+
+int li_device_status(void *stream)
+{
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return LI_ERR_CUDA;
+    int *p = device_status_ptr();
+    if (!p)
+        return LI_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpy(&v, p, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return LI_ERR_CUDA;
+    if (v != 0 && cudaMemset(p, 0, sizeof v) != cudaSuccess)
+        return LI_ERR_CUDA;
+    return v;
+}
+
+} // extern "C"

@@ -1,0 +1,79 @@
+// li_internal.cuh -- kernel parameter blocks and launchers shared by the
+// library's translation units (not part of the public ABI).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "../../include/li.h"
+
+namespace li {
+
+// Upper bound for any single mbarrier wait inside a kernel (ns).
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+// ------------------------------------------------------------- absorption
+struct AbsorbParams {
+    const void *q;        // [N][G][H][d]
+    const void *D;        // [G][r][d] or nullptr (identity)
+    void *q_abs;          // [N][G][H][r]
+    float *q_abs_scale;   // [N][G][H] (fp8 only)
+    int q_t, D_t, abs_t;
+    int N, G, H, d, r;
+};
+cudaError_t launch_absorb(const AbsorbParams &p, cudaStream_t s);
+
+// ------------------------------------------------------------- scoring
+// One scoring launch evaluates eq. (8) for a contiguous range of Gs layers
+// [g0, g0 + Gs) of a group of Gtot layers, either over every cached token
+// (scan mode) or over a per-sequence list of gathered token indices.
+struct ScoreParams {
+    const void *latent;          // [B][L_lat][r]
+    const float *lat_scale;      // [B][L_lat] or nullptr
+    const void *q_abs;           // [B][T][Gtot][H][r]
+    const float *q_abs_scale;    // [B][T][Gtot][H] or nullptr
+    const float *w;              // [B][T][Gtot][H]
+    const float *beta;           // [B][T][Gtot][H] or nullptr
+    const int32_t *q_pos;        // [T] or nullptr (scan mode only)
+    const int32_t *gather_idx;   // [B][L_out] or nullptr (gather mode)
+    float *scores;               // [B][T][Gs][L_out]
+    int *status;
+    int lat_t, abs_t;
+    int B, T, Gtot, g0, Gs, H, r;
+    int L_lat;                   // cached tokens per sequence
+    int L_out;                   // positions per score row (scan: L_lat; gather: m)
+    int n_gather;                // valid gathered positions (gather mode)
+};
+cudaError_t launch_score_simt(const ScoreParams &p, cudaStream_t s);
+bool score_tc_supported(const ScoreParams &p);
+cudaError_t launch_score_tc(const ScoreParams &p, cudaStream_t s);
+
+// ------------------------------------------------------------- selection
+// Row r of the input is scores + r * in_stride, with valid length
+// valid_len[r] (or L_row); its selection goes to out row
+//   (r / rows_per_group) * group_stride + (r % rows_per_group) + row_offset
+// of idx/vals (each out row holds k entries).  When `map` is set, selected
+// positions j are written as map[(r / rows_per_group) * map_stride + j].
+struct TopkParams {
+    const float *scores;
+    int64_t rows;
+    int64_t in_stride;
+    int L_row;
+    const int32_t *valid_len;
+    int k;
+    int32_t *idx;
+    float *vals;
+    int rows_per_group, group_stride, row_offset;
+    const int32_t *map;
+    int64_t map_stride;
+    int *status;
+};
+cudaError_t launch_topk(const TopkParams &p, cudaStream_t s);
+
+// Per-device status word (address of the __device__ variable on the current
+// device), or nullptr on failure.
+int *device_status_ptr();
+
+} // namespace li

@@ -1,0 +1,126 @@
+"""Host-side checks of the C ABI (CPU only, no CUDA call is made).
+
+The library must load, export every function include/li.h declares, and
+reject bad arguments with the documented status *before* touching CUDA --
+so these run on a machine without a GPU.  Fake device addresses are plain
+integers that are never dereferenced.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "li.h")
+
+LI_OK, LI_ERR_INVALID_ARG, LI_ERR_ALIGNMENT, LI_ERR_UNSUPPORTED, LI_ERR_WORKSPACE = 0, -1, -2, -3, -4
+F32, BF16, FP8 = 0, 1, 2
+A = 0x10000      # a fake, 16-byte aligned "device" address (never dereferenced)
+MIS = 0x10004    # misaligned
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(li_[a-z_0-9]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    import shared_latent_key_cache_b300 as m
+    return m.lib()
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("li_absorb_queries", "li_score_group", "li_topk", "li_hs_select",
+              "li_native_score", "li_hs_workspace_size", "li_device_status", "li_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for n in declared_functions():
+        assert hasattr(L, n), f"{n} declared in li.h but not exported"
+
+
+def test_exports_are_c_symbols():
+    so = os.path.join(ROOT, "shared_latent_key_cache_b300", "libli_b300.so")
+    lib = ctypes.CDLL(so)
+    for n in declared_functions():
+        getattr(lib, n)   # unmangled lookup succeeds only for extern "C" symbols
+
+
+def test_version_and_status_strings(L):
+    assert L.li_version() >= 100
+    for s in (0, -1, -2, -3, -4, -5, -6, -7):
+        assert L.li_status_string(s).startswith(b"LI_")
+    assert L.li_status_string(12345) == b"unknown status"
+
+
+def _score(lib, **kw):
+    a = dict(latent=A, lat_t=BF16, lat_scale=None, q_abs=A, abs_t=BF16, q_abs_scale=None, w=A,
+             beta=None, q_pos=None, B=1, T=1, G=4, H=64, r=192, Lc=1000, scores=A)
+    a.update(kw)
+    return lib.li_score_group(a["latent"], a["lat_t"], a["lat_scale"], a["q_abs"], a["abs_t"],
+                            a["q_abs_scale"], a["w"], a["beta"], a["q_pos"], a["B"], a["T"], a["G"],
+                            a["H"], a["r"], a["Lc"], a["scores"], None)
+
+
+def test_score_group_argument_errors(L):
+    assert _score(L, latent=None) == LI_ERR_INVALID_ARG
+    assert _score(L, scores=None) == LI_ERR_INVALID_ARG
+    assert _score(L, w=None) == LI_ERR_INVALID_ARG
+    assert _score(L, lat_t=7) == LI_ERR_INVALID_ARG
+    assert _score(L, Lc=0) == LI_ERR_INVALID_ARG
+    assert _score(L, H=-1) == LI_ERR_INVALID_ARG
+    assert _score(L, lat_t=FP8, abs_t=FP8, q_abs_scale=A) == LI_ERR_INVALID_ARG  # fp8 needs lat_scale
+    assert _score(L, lat_t=FP8, abs_t=FP8, lat_scale=A) == LI_ERR_INVALID_ARG    # and q_abs_scale
+    assert _score(L, latent=MIS) == LI_ERR_ALIGNMENT
+    assert _score(L, beta=MIS) == LI_ERR_ALIGNMENT
+    assert _score(L, r=512) == LI_ERR_UNSUPPORTED
+    assert _score(L, G=64, H=128, r=256) == LI_ERR_UNSUPPORTED   # too big for either kernel
+
+
+def test_absorb_argument_errors(L):
+    f = L.li_absorb_queries
+    assert f(None, BF16, A, BF16, 1, 1, 4, 64, 128, 192, A, BF16, None, None) == LI_ERR_INVALID_ARG
+    assert f(A, FP8, A, BF16, 1, 1, 4, 64, 128, 192, A, BF16, None, None) == LI_ERR_INVALID_ARG
+    assert f(A, BF16, None, BF16, 1, 1, 4, 64, 128, 192, A, BF16, None, None) == LI_ERR_INVALID_ARG  # D=NULL needs r==d
+    assert f(A, BF16, A, BF16, 1, 1, 4, 64, 128, 192, A, FP8, None, None) == LI_ERR_INVALID_ARG     # fp8 needs scale
+    assert f(A, BF16, MIS, BF16, 1, 1, 4, 64, 128, 192, A, BF16, None, None) == LI_ERR_ALIGNMENT
+    assert f(A, BF16, A, BF16, 1, 1, 4, 64, 128, 300, A, BF16, None, None) == LI_ERR_UNSUPPORTED
+
+
+def test_topk_argument_errors(L):
+    f = L.li_topk
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
+                  ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+    assert f(None, 4, 100, None, 10, A, None, None) == LI_ERR_INVALID_ARG
+    assert f(A, 4, 100, None, 0, A, None, None) == LI_ERR_INVALID_ARG
+    assert f(A, -1, 100, None, 10, A, None, None) == LI_ERR_INVALID_ARG
+    assert f(MIS, 4, 100, None, 10, A, None, None) == LI_ERR_ALIGNMENT
+    assert f(A, 0, 100, None, 10, A, None, None) == LI_OK        # nothing to do, no CUDA call
+
+
+def test_hs_workspace_size_and_errors(L):
+    ws = L.li_hs_workspace_size(8, 4, 131072, 8192, 2048)
+    assert ws == 8 * 131072 * 4 + 8 * 8192 * 4 + 8 * 3 * 8192 * 4
+    assert L.li_hs_workspace_size(0, 4, 10, 10, 10) == 0
+    f = L.li_hs_select
+    args = [A, FP8, A, A, FP8, A, A, None, 2, 4, 64, 192, 1000, 256, 64, A, A, A, ws, None]
+    bad_mk = list(args); bad_mk[13] = 32          # m < k
+    assert f(*bad_mk) == LI_ERR_INVALID_ARG
+    no_ws = list(args); no_ws[17] = None
+    assert f(*no_ws) == LI_ERR_WORKSPACE
+    small = list(args); small[18] = 16
+    assert f(*small) == LI_ERR_WORKSPACE
+    mis_ws = list(args); mis_ws[17] = A + 16
+    assert f(*mis_ws) == LI_ERR_ALIGNMENT
+
+
+def test_native_argument_errors(L):
+    f = L.li_native_score
+    assert f(None, FP8, A, A, FP8, A, A, 1, 64, 128, 100, A, None) == LI_ERR_INVALID_ARG
+    assert f(A, FP8, None, A, FP8, A, A, 1, 64, 128, 100, A, None) == LI_ERR_INVALID_ARG
+    assert f(A, FP8, A, A, FP8, A, A, 1, 64, 128, 0, A, None) == LI_ERR_INVALID_ARG

@@ -1,0 +1,308 @@
+"""GPU parity of each kernel against the CPU oracle on small seeded cases.
+
+Every call goes through the C ABI (ctypes binding); inputs come from
+li_inputs, expected values from the oracle only.  Sizes span several
+128-token tiles plus a ragged tail and stay small enough for the oracle to
+finish in seconds.
+"""
+import numpy as np
+import pytest
+import torch
+
+import li_inputs
+from parity import RTOL, assert_scores_close, assert_topk_row, exact_sets_equal, max_rel_err
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+def _dev(x):
+    return None if x is None else x.to(DEV)
+
+
+def _sync_ok(li):
+    assert li.li_device_status() == 0
+
+
+# ------------------------------------------------------------------ absorption
+
+@pytest.mark.parametrize("abs_dtype", ["f32", "bf16", "fp8"])
+@pytest.mark.parametrize("q_dtype", ["f32", "bf16"])
+def test_absorb_matches_oracle(li, orc, q_dtype, abs_dtype):
+    w = li_inputs.spec("dsa_bf16_8k", B=3, T=2, L=8, q_dtype=q_dtype, native=False)
+    x = li_inputs.make_workload(w, seed=1)
+    q_abs, scale = li.absorb_queries(_dev(x["q"]), _dev(x["D"]), abs_dtype)
+    _sync_ok(li)
+    o = orc.absorb(x["q"], x["D"])                                     # fp64
+    if abs_dtype == "fp8":
+        g = orc.decode_rows(q_abs.cpu(), scale.cpu())
+        amax = np.abs(o).max(axis=-1)
+        np.testing.assert_allclose(scale.cpu().numpy(), amax / 448.0, rtol=1e-5)
+        # one E4M3 rounding: |err| <= 2^-4 |o| (normal range) or half the
+        # subnormal spacing (2^-10 of the scale * 448... = s * 2^-10), plus fp32 accumulation
+        s = scale.cpu().numpy()[..., None]
+        tol = 2.0 ** -4 * np.abs(o) + s * 2.0 ** -10 + 1e-5 * amax[..., None]
+        assert (np.abs(g - o) <= tol).all()
+    elif abs_dtype == "bf16":
+        g = q_abs.float().cpu().double().numpy()
+        assert (np.abs(g - o) <= 2.0 ** -8 * np.abs(o) + 1e-6 * np.abs(o).max()).all()
+    else:
+        g = q_abs.cpu().double().numpy()
+        np.testing.assert_allclose(g, o, rtol=1e-5, atol=1e-6 * np.abs(o).max())
+
+
+def test_absorb_identity_decoder_is_a_conversion(li):
+    q = torch.randn(2, 1, 1, 64, 128, generator=torch.Generator().manual_seed(3)).to(torch.bfloat16)
+    q_abs, _ = li.absorb_queries(q.to(DEV), None, "bf16")
+    assert torch.equal(q_abs.cpu(), q)
+    q32, _ = li.absorb_queries(q.float().to(DEV), None, "f32")
+    assert torch.equal(q32.cpu(), q.float())
+    q8, s8 = li.absorb_queries(q.to(DEV), None, "fp8")
+    ref_codes, ref_scale = li_inputs.quantize_rows_fp8(q.float())
+    np.testing.assert_allclose(s8.cpu().numpy(), ref_scale.numpy(), rtol=1e-6)
+    # same RNE rounding of the same quotient, up to a one-ulp difference in x/s
+    d = (q8.cpu().view(torch.float8_e4m3fn).float() - ref_codes.view(torch.float8_e4m3fn).float()).abs()
+    assert (d <= ref_codes.view(torch.float8_e4m3fn).float().abs() * 2.0 ** -3 + 1e-6).all()
+
+
+# --------------------------------------------------------------------- scoring
+
+def _score_case(li, orc, lat_dtype, B, T, G, H, r, L, seed=0, beta=False, q_pos=None):
+    lat, lsc, _ = li_inputs.make_latent(B, L, r, lat_dtype, seed=seed)
+    qa, qs = li_inputs.make_absorbed_queries(B, T, G, H, r, lat_dtype if lat_dtype != "f32" else "f32",
+                                             seed=seed)
+    w = torch.rand(B, T, G, H, generator=torch.Generator().manual_seed(seed + 7))
+    bt = li_inputs.make_beta(B, T, G, H, seed=seed) if beta else None
+    g = li.score_group(_dev(lat), _dev(lsc), _dev(qa), _dev(qs), _dev(w), beta=_dev(bt),
+                       q_pos=_dev(q_pos))
+    _sync_ok(li)
+    o = orc.score(lat, lsc, orc.decode_rows(qa, qs), w, beta=bt, q_pos=q_pos)
+    return g.cpu().double().numpy(), o
+
+
+@pytest.mark.parametrize("L", [1, 127, 128, 129, 1000])
+def test_score_f32_simt(li, orc, L):
+    g, o = _score_case(li, orc, "f32", B=2, T=1, G=4, H=8, r=32, L=L)
+    assert_scores_close(g, o, RTOL["f32"])
+
+
+@pytest.mark.parametrize("dt", ["bf16", "fp8"])
+@pytest.mark.parametrize("L", [1, 127, 128, 129, 1000, 3000])
+def test_score_tensor_core(li, orc, dt, L):
+    g, o = _score_case(li, orc, dt, B=2, T=1, G=4, H=64, r=192, L=L, seed=L)
+    assert_scores_close(g, o, RTOL[dt])
+    # both sides consume identical operands: only fp32 accumulation order differs
+    assert max_rel_err(g, o) < 1e-4
+
+
+@pytest.mark.parametrize("dt", ["bf16", "fp8"])
+@pytest.mark.parametrize("G,H,r", [(1, 64, 192), (3, 64, 128), (2, 128, 64), (4, 32, 256), (8, 16, 64)])
+def test_score_tensor_core_shapes(li, orc, dt, G, H, r):
+    g, o = _score_case(li, orc, dt, B=3, T=1, G=G, H=H, r=r, L=777, seed=G * 100 + H)
+    assert_scores_close(g, o, RTOL[dt])
+    assert max_rel_err(g, o) < 1e-4
+
+
+@pytest.mark.parametrize("dt", ["bf16", "fp8"])
+def test_score_with_beta(li, orc, dt):
+    g, o = _score_case(li, orc, dt, B=2, T=1, G=4, H=64, r=192, L=600, seed=5, beta=True)
+    assert_scores_close(g, o, RTOL[dt])
+    assert max_rel_err(g, o) < 1e-4
+
+
+def test_score_f32_with_beta(li, orc):
+    g, o = _score_case(li, orc, "f32", B=2, T=1, G=4, H=8, r=32, L=300, seed=6, beta=True)
+    assert_scores_close(g, o, RTOL["f32"])
+
+
+@pytest.mark.parametrize("dt", ["bf16", "fp8", "f32"])
+def test_score_causal_prefill(li, orc, dt):
+    """Query t sees s <= q_pos[t]; entries past the limit are left untouched."""
+    B, T, L = 2, 5, 700
+    G, H, r = (4, 64, 192) if dt != "f32" else (4, 8, 32)
+    q_pos = torch.tensor([0, 127, 128, 400, 699], dtype=torch.int32)
+    lat, lsc, _ = li_inputs.make_latent(B, L, r, dt, seed=9)
+    qa, qs = li_inputs.make_absorbed_queries(B, T, G, H, r, dt, seed=9)
+    w = torch.rand(B, T, G, H, generator=torch.Generator().manual_seed(2))
+    out = torch.full((B, T, G, L), float("nan"), device=DEV)
+    li.score_group(_dev(lat), _dev(lsc), _dev(qa), _dev(qs), _dev(w), q_pos=_dev(q_pos), out=out)
+    _sync_ok(li)
+    o = orc.score(lat, lsc, orc.decode_rows(qa, qs), w, q_pos=q_pos)
+    g = out.cpu().double().numpy()
+    for t, p in enumerate(q_pos.tolist()):
+        assert_scores_close(g[:, t, :, :p + 1], o[:, t, :, :p + 1], RTOL[dt], f"query {t}")
+        assert np.isnan(g[:, t, :, p + 1:]).all(), "wrote past the causal limit"
+
+
+def test_score_mixed_dtypes_fall_back_to_cuda_cores(li, orc):
+    """bf16 latent with fp8 absorbed queries (no tensor-core form) still scores exactly."""
+    B, L, G, H, r = 1, 300, 2, 16, 64
+    lat, _, _ = li_inputs.make_latent(B, L, r, "bf16", seed=4)
+    qa, qs = li_inputs.make_absorbed_queries(B, 1, G, H, r, "fp8", seed=4)
+    w = torch.rand(B, 1, G, H, generator=torch.Generator().manual_seed(4))
+    g = li.score_group(_dev(lat), None, _dev(qa), _dev(qs), _dev(w)).cpu().double().numpy()
+    o = orc.score(lat, None, orc.decode_rows(qa, qs), w)
+    assert_scores_close(g, o, 1e-5)
+
+
+# ---------------------------------------------------------------------- top-k
+
+def _topk_gpu(li, s, k, valid_len=None):
+    idx, vals = li.topk(s.to(DEV), k, valid_len=_dev(valid_len), with_vals=True)
+    _sync_ok(li)
+    return idx.cpu().numpy(), vals.cpu().numpy()
+
+
+@pytest.mark.parametrize("L,k", [(1, 1), (5, 3), (100, 100), (100, 250), (4096, 256),
+                                 (8192, 2048), (32768, 2048), (131072, 8192)])
+def test_topk_bit_exact_random(li, orc, L, k):
+    s = torch.randn(3, L, generator=torch.Generator().manual_seed(L + k)) * 5 + 10
+    gi, gv = _topk_gpu(li, s, k)
+    oi, ov = orc.topk(s.double().numpy(), k)
+    exact_sets_equal(gi, oi)
+    n = min(k, L)
+    np.testing.assert_array_equal(np.sort(gv[:, :n], axis=1), np.sort(ov[:, :n].astype(np.float32), axis=1))
+
+
+def test_topk_ties_take_lowest_positions(li, orc):
+    g = torch.Generator().manual_seed(11)
+    s = torch.randint(-3, 4, (8, 5000), generator=g).float()          # massive ties
+    s[1] = 2.0                                                        # all equal
+    s[2, ::7] = -0.0
+    for k in (1, 17, 1024, 4999):
+        gi, _ = _topk_gpu(li, s, k)
+        oi, _ = orc.topk(s.double().numpy(), k)
+        exact_sets_equal(gi, oi)
+
+
+def test_topk_threshold_bin_overflows_shared_memory(li, orc):
+    """Scores sharing their top 12 key bits (one exponent, same 3 mantissa bits) force the
+    re-read path; a narrower cluster forces the second-digit re-read too."""
+    g = torch.Generator().manual_seed(12)
+    wide = 1.0 + torch.rand(2, 100000, generator=g) * 0.12
+    narrow = 1.0 + torch.rand(2, 100000, generator=g) * 1e-4
+    for s in (wide, narrow):
+        for k in (10, 5000, 60000):
+            gi, _ = _topk_gpu(li, s, k)
+            oi, _ = orc.topk(s.double().numpy(), k)
+            exact_sets_equal(gi, oi)
+
+
+def test_topk_valid_len_and_padding(li, orc):
+    s = torch.randn(6, 3000, generator=torch.Generator().manual_seed(13))
+    vl = torch.tensor([0, 1, 100, 2999, 3000, 5000], dtype=torch.int32)
+    gi, gv = _topk_gpu(li, s, 200, vl)
+    oi, _ = orc.topk(s.double().numpy(), 200, valid_len=vl.numpy())
+    exact_sets_equal(gi, oi)
+    assert (gi[0] == -1).all() and np.isneginf(gv[0]).all()
+    assert gi[1, 0] == 0 and (gi[1, 1:] == -1).all()
+
+
+def test_topk_negative_and_infinite_scores(li, orc):
+    s = torch.randn(4, 2000, generator=torch.Generator().manual_seed(14)) - 50
+    s[0, :1500] = float("-inf")
+    s[1, 100] = float("inf")
+    gi, _ = _topk_gpu(li, s, 700)
+    oi, _ = orc.topk(s.double().numpy(), 700)
+    exact_sets_equal(gi, oi)
+
+
+# ---------------------------------------------------------------- pipelines
+
+@pytest.mark.parametrize("name", ["tiny_f32", "dsa_bf16_8k"])
+def test_pipeline_full_workload(li, orc, name):
+    """absorb -> score -> top-k on the GPU vs the oracle's fp64 absorb -> score -> TopK."""
+    x = li_inputs.make_workload(name, seed=0)
+    w = x["spec"]
+    absd = {"f32": "f32", "bf16": "bf16", "fp8": "fp8"}[w.lat_dtype]
+    qa, qs = li.absorb_queries(_dev(x["q"]), _dev(x["D"]), absd)
+    s = li.score_group(_dev(x["latent"]), _dev(x["lat_scale"]), qa, qs, _dev(x["w"]))
+    idx = li.topk(s, w.k)
+    _sync_ok(li)
+    o = orc.score(x["latent"], x["lat_scale"], orc.absorb(x["q"], x["D"]), x["w"])
+    rt = RTOL[w.lat_dtype]
+    assert_scores_close(s.cpu().numpy(), o, rt)
+    gi = idx.cpu().numpy()
+    for b in range(w.B):
+        for l in range(w.G):
+            assert_topk_row(gi[b, 0, l], o[b, 0, l], w.k, w.L, rt, f"b{b} l{l}")
+
+
+def test_pipeline_fp8_reduced_batch(li, orc):
+    w = li_inputs.spec("fp8_32k_b32", B=3, L=5000, native=False)
+    x = li_inputs.make_workload(w, seed=2)
+    qa, qs = li.absorb_queries(_dev(x["q"]), _dev(x["D"]), "fp8")
+    s = li.score_group(_dev(x["latent"]), _dev(x["lat_scale"]), qa, qs, _dev(x["w"]))
+    idx = li.topk(s, w.k)
+    _sync_ok(li)
+    o = orc.score(x["latent"], x["lat_scale"], orc.absorb(x["q"], x["D"]), x["w"])
+    assert_scores_close(s.cpu().numpy(), o, RTOL["fp8"])
+    gi = idx.cpu().numpy()
+    for b in range(w.B):
+        for l in range(w.G):
+            assert_topk_row(gi[b, 0, l], o[b, 0, l], w.k, w.L, RTOL["fp8"], f"b{b} l{l}")
+
+
+# ------------------------------------------------------------------- native
+
+def test_native_scan_matches_oracle(li, orc):
+    x = li_inputs.make_workload(li_inputs.spec("dsa_bf16_8k", B=2, L=3000), seed=3)
+    w = x["spec"]
+    for l in range(w.G):
+        q8, s8 = li.absorb_queries(_dev(x["q"][:, :, l:l + 1]), None, "fp8")
+        g = li.native_score(_dev(x["keys"][l]), _dev(x["key_scale"][l]), q8.view(w.B, w.H, w.d),
+                            s8.view(w.B, w.H), _dev(x["w"][:, 0, l]))
+        _sync_ok(li)
+        o = orc.native_score(x["keys"][l], x["key_scale"][l], orc.decode_rows(x["q"][:, 0, l]),
+                             x["w"][:, 0, l])
+        assert_scores_close(g.cpu().numpy(), o, RTOL["fp8"])
+
+
+# ----------------------------------------------------------------------- HS
+
+def _hs_check(li, orc, x, m, k, dt):
+    w = x["spec"]
+    absd = "fp8" if dt == "fp8" else "bf16"
+    qa, qs = li.absorb_queries(_dev(x["q"]), _dev(x["D"]), absd)
+    cand, idx = li.hs_select(_dev(x["latent"]), _dev(x["lat_scale"]), qa, qs, _dev(x["w"]), m, k)
+    _sync_ok(li)
+    o = orc.score(x["latent"], x["lat_scale"], orc.absorb(x["q"], x["D"]), x["w"])[:, 0]  # [B][G][L]
+    c = cand.cpu().numpy()
+    gi = idx.cpu().numpy()
+    rt = RTOL[dt]
+    nc = min(m, w.L)
+    for b in range(w.B):
+        assert_topk_row(c[b], o[b, 0], m, w.L, rt, f"cand b{b}")
+        C = set(c[b, :nc].tolist())
+        for l in range(w.G):
+            assert_topk_row(gi[b, l], o[b, l], k, w.L if l == 0 else w.L, rt, f"b{b} l{l}",
+                            allowed=C)
+    return c, gi, o
+
+
+@pytest.mark.parametrize("dt", ["bf16", "fp8"])
+def test_hs_matches_oracle(li, orc, dt):
+    w = li_inputs.spec("fp8_128k_hs", B=2, L=3000, m=512, k=128, lat_dtype=dt)
+    x = li_inputs.make_workload(w, seed=4)
+    _hs_check(li, orc, x, 512, 128, dt)
+
+
+def test_hs_budget_at_least_context_is_full_latentindex(li, orc):
+    w = li_inputs.spec("fp8_128k_hs", B=2, L=900, m=1024, k=100)
+    x = li_inputs.make_workload(w, seed=5)
+    c, gi, o = _hs_check(li, orc, x, 1024, 100, "fp8")
+    assert (c[:, 900:] == -1).all()
+    for b in range(2):
+        assert sorted(c[b, :900].tolist()) == list(range(900))
+        for l in range(w.G):
+            assert_topk_row(gi[b, l], o[b, l], 100, 900, RTOL["fp8"], f"full b{b} l{l}")
+
+
+def test_hs_budget_equal_k_gives_candidates(li, orc):
+    w = li_inputs.spec("fp8_128k_hs", B=2, L=2000, m=256, k=256)
+    x = li_inputs.make_workload(w, seed=6)
+    c, gi, _ = _hs_check(li, orc, x, 256, 256, "fp8")
+    for b in range(2):
+        for l in range(w.G):
+            assert set(gi[b, l].tolist()) == set(c[b].tolist())
