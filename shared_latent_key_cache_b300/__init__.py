@@ -43,7 +43,7 @@ def _load():
     if not os.path.exists(library_path):
         raise ImportError(
             f"{library_path} is missing: build it with "
-            "`python -m shared_latent_key_cache_b300._build` (nvcc, sm_103a)")
+            "`python shared_latent_key_cache_b300/_build.py` (nvcc, sm_103a)")
     L = ctypes.CDLL(library_path)
     P, I, I64, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
     L.li_version.restype = I

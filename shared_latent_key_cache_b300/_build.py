@@ -1,6 +1,6 @@
 """Builds libli_b300.so in-tree from csrc/*.cu with nvcc for sm_103a.
 
-    python -m shared_latent_key_cache_b300._build [--force] [--verbose]
+    python shared_latent_key_cache_b300/_build.py [--force] [--verbose]
 
 Each translation unit is compiled separately (in parallel) with
 ``-gencode arch=compute_103a,code=sm_103a -lineinfo -O3`` and linked into one

@@ -17,7 +17,7 @@
 // the inner loop (w s_q is precomputed per query, s_c applied once per token).
 // With beta the scales are applied before the ReLU.
 //
-// Roles of the 256 threads (one persistent CTA per SM, static contiguous
+// Roles of the 384 threads (one persistent CTA per SM, static contiguous
 // split of the (query, 128-token tile) work units):
 //   warp 0      TMA producer: latent tiles -> smem ring (and the query
 //               operand whenever the work unit's query changes)
@@ -25,8 +25,11 @@
 //   warps 2-3   gather mode only: with warp 0, copy gathered latent rows
 //               into the swizzled smem layout (HS followers rescoring the
 //               anchor's candidates)
-//   warps 4-7   epilogue: TMEM -> registers, ReLU, weighted head sums,
-//               per-token scale, score stores
+//   warps 4-11  epilogue, two warps per TMEM lane quarter (warp % 4), each
+//               taking half of the layers: TMEM -> registers 32 columns at a
+//               time (the next chunk's load in flight while the current one
+//               is reduced), ReLU, weighted head sums with packed fp32 FMA,
+//               per-token scale, one coalesced score store per layer
 // The two TMEM accumulators are double-buffered so the epilogue of tile i
 // overlaps the MMAs of tile i+1 and the loads of the tiles after it.
 //
@@ -45,7 +48,8 @@
 namespace li {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;
+constexpr int kEpiWarps = 8;
 constexpr int kTileM = 128;
 constexpr int kChunkElems = 64;
 constexpr int kMaxDev = 64;
@@ -76,11 +80,12 @@ struct Misc {
     uint32_t tmem_base;
     int abort;
     int pad[2];
-    // per-epilogue-warp copies of the current query's head constants, so that
-    // no cross-warp barrier is needed when the query changes
-    float wq[4][256];
-    float sq[4][256];
-    float bq[4][256];
+    // per-epilogue-warp copies of the current query's head constants for the
+    // warp's layers (<= 128 columns), so no cross-warp barrier is needed when
+    // the query changes
+    float wq[kEpiWarps][128];
+    float sq[kEpiWarps][128];
+    float bq[kEpiWarps][128];
 };
 
 // One lane polls, the whole warp gets the (uniform) outcome.
@@ -91,6 +96,27 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volati
     if ((threadIdx.x & 31) == 0)
         ok = mbar_wait(bar, parity, abort, status, kWaitLimitNs);
     return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+}
+
+// Walks a CTA's contiguous range of (query row bt, 128-token tile) work units
+// without a 64-bit division per unit.
+struct UnitIter {
+    int64_t bt;
+    int tile;
+    int NT;
+    __device__ __forceinline__ UnitIter(int64_t u, int nt) : bt(u / nt), tile(static_cast<int>(u % nt)), NT(nt) {}
+    __device__ __forceinline__ void next()
+    {
+        if (++tile == NT) {
+            tile = 0;
+            ++bt;
+        }
+    }
+};
+
+__device__ __forceinline__ int seq_of(int64_t bt, int T)
+{
+    return T == 1 ? static_cast<int>(bt) : static_cast<int>(bt / T);
 }
 
 template <bool kGather>
@@ -145,7 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bars->done, 1u);
         for (int a = 0; a < 2; ++a) {
             mbar_init(&bars->tmem_full[a], 1u);
-            mbar_init(&bars->tmem_empty[a], 4u);
+            mbar_init(&bars->tmem_empty[a], static_cast<uint32_t>(kEpiWarps));
         }
         misc->abort = 0;
         mbar_fence_init();
@@ -170,9 +196,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             int nb = 0;
             uint32_t last_par[8] = {0, 0, 0, 0, 0, 0, 0, 0};
             bool used[8] = {false, false, false, false, false, false, false, false};
-            for (int64_t u = u_begin; u < u_end; ++u) {
-                const int64_t bt = u / c.NT;
-                const int tile = static_cast<int>(u % c.NT);
+            UnitIter it(u_begin, c.NT);
+            for (int64_t u = u_begin; u < u_end; ++u, it.next()) {
+                const int64_t bt = it.bt;
+                const int tile = it.tile;
                 if (tile * kTileM >= unit_valid_len<kGather>(p, bt))
                     continue;
                 if (bt != cur_bt) {
@@ -192,7 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 uint8_t *dstA = smA + stage * c.a_stage_bytes;
                 mbar_arrive_expect_tx(&full[stage], static_cast<uint32_t>(c.a_stage_bytes));
-                const int b = static_cast<int>(bt / p.T);
+                const int b = seq_of(bt, p.T);
                 for (int ch = 0; ch < c.nchunk; ++ch)
                     tma_load_3d(dstA + ch * c.a_chunk_bytes, &tmA, &full[stage], ch * kChunkElems,
                                 tile * kTileM, b);
@@ -227,12 +254,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int pieces_per_row = c.nchunk * kPiecesPerChunk;
         const int total = kTileM * pieces_per_row;
         const uint8_t *lat = static_cast<const uint8_t *>(p.latent);
-        for (int64_t u = u_begin; u < u_end; ++u) {
-            const int64_t bt = u / c.NT;
-            const int tile = static_cast<int>(u % c.NT);
+        UnitIter it(u_begin, c.NT);
+        for (int64_t u = u_begin; u < u_end; ++u, it.next()) {
+            const int64_t bt = it.bt;
+            const int tile = it.tile;
             if (tile * kTileM >= unit_valid_len<kGather>(p, bt))
                 continue;
-            const int b = static_cast<int>(bt / p.T);
+            const int b = seq_of(bt, p.T);
             if (bt != cur_bt) {
                 if (warp == 0) {
                     bool ok = true;
@@ -305,9 +333,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t acc_phase = 0;
             int64_t cur_bt = -1;
             int nb = 0;
-            for (int64_t u = u_begin; u < u_end; ++u) {
-                const int64_t bt = u / c.NT;
-                const int tile = static_cast<int>(u % c.NT);
+            UnitIter it(u_begin, c.NT);
+            for (int64_t u = u_begin; u < u_end; ++u, it.next()) {
+                const int64_t bt = it.bt;
+                const int tile = it.tile;
                 if (tile * kTileM >= unit_valid_len<kGather>(p, bt))
                     continue;
                 if (bt != cur_bt) {
@@ -357,25 +386,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp >= 4) {
         // ------------------------------------------------------------ epilogue
-        const int ew = warp - 4;                       // TMEM lane quarter
-        const int row = ew * 32 + lane;
-        float *wq = misc->wq[ew];
-        float *sq = misc->sq[ew];
-        float *bq = misc->bq[ew];
+        constexpr int CH = kH < 32 ? kH : 32;          // TMEM columns per load
+        constexpr int CPL = kH / CH;                   // loads per layer
+        const int e = warp - 4;                        // 0..7
+        const int quarter = warp & 3;                  // TMEM lane quarter
+        const int lper = (Gs + 1) / 2;
+        const int l_begin = (e >> 2) * lper;
+        const int l_end = min(Gs, l_begin + lper);
+        const int nlay = l_end > l_begin ? l_end - l_begin : 0;
+        const int nchunks = nlay * CPL;
+        const int row = quarter * 32 + lane;
+        float *wq = misc->wq[e];
+        float *sq = misc->sq[e];
+        float *bq = misc->bq[e];
         int acc = 0;
         uint32_t acc_phase = 0;
         int64_t cur_bt = -1;
-        for (int64_t u = u_begin; u < u_end; ++u) {
-            const int64_t bt = u / c.NT;
-            const int tile = static_cast<int>(u % c.NT);
+        UnitIter it(u_begin, c.NT);
+        for (int64_t u = u_begin; u < u_end; ++u, it.next()) {
+            const int64_t bt = it.bt;
+            const int tile = it.tile;
             const int Lv = unit_valid_len<kGather>(p, bt);
             if (tile * kTileM >= Lv)
                 continue;
-            const int b = static_cast<int>(bt / p.T);
+            const int b = seq_of(bt, p.T);
             if (bt != cur_bt) {
                 __syncwarp();
-                const int64_t wrow = (bt * p.Gtot + p.g0) * p.H;
-                for (int j = lane; j < c.N; j += 32) {
+                const int64_t wrow = (bt * p.Gtot + p.g0 + l_begin) * p.H;
+                for (int j = lane; j < nlay * kH; j += 32) {
                     const float wv = p.w[wrow + j];
                     const float sv = p.q_abs_scale ? p.q_abs_scale[wrow + j] : 1.f;
                     if (kBeta) {
@@ -405,33 +443,59 @@ __global__ void __launch_bounds__(kThreads, 1)
                         sc = p.lat_scale[static_cast<int64_t>(b) * p.L_lat + tok];
                 }
             }
-            const uint32_t trow = tmem_base + (static_cast<uint32_t>(ew * 32) << 16) +
-                                  static_cast<uint32_t>(acc * c.acc_stride);
-            float *out = p.scores + bt * Gs * static_cast<int64_t>(p.L_out) + pos;
-            for (int l = 0; l < Gs; ++l) {
-                float part[4] = {0.f, 0.f, 0.f, 0.f};
+            const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                   static_cast<uint32_t>(acc * c.acc_stride + l_begin * kH);
+            float *out = p.scores + (bt * Gs + l_begin) * static_cast<int64_t>(p.L_out) + pos;
+
+            float2 s2a = make_float2(0.f, 0.f), s2b = make_float2(0.f, 0.f);
+            // reduce one chunk of CH head columns into the running layer sum
+            auto consume = [&](int i, const uint32_t (&v)[CH]) {
+                const int col = i * CH;
+                if (kBeta) {
 #pragma unroll
-                for (int hc = 0; hc < kH / 16; ++hc) {
-                    uint32_t v[16];
-                    const int col = l * kH + hc * 16;
-                    tmem_ld16(trow + static_cast<uint32_t>(col), v);
-                    tmem_ld_wait16(v);
+                    for (int j = 0; j < CH; j += 2) {
+                        const float x0 = fmaf(__uint_as_float(v[j]) * sq[col + j], sc, bq[col + j]);
+                        const float x1 = fmaf(__uint_as_float(v[j + 1]) * sq[col + j + 1], sc, bq[col + j + 1]);
+                        s2a = __ffma2_rn(make_float2(wq[col + j], wq[col + j + 1]),
+                                         make_float2(fmaxf(x0, 0.f), fmaxf(x1, 0.f)), s2a);
+                    }
+                } else {
+                    const float4 *w4 = reinterpret_cast<const float4 *>(wq + col);
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const float a = __uint_as_float(v[j]);
-                        if (kBeta) {
-                            const float x = fmaf(a * sq[col + j], sc, bq[col + j]);
-                            part[j & 3] = fmaf(wq[col + j], fmaxf(x, 0.f), part[j & 3]);
-                        } else {
-                            part[j & 3] = fmaf(wq[col + j], fmaxf(a, 0.f), part[j & 3]);
-                        }
+                    for (int j = 0; j < CH; j += 4) {
+                        const float4 ww = w4[j / 4];
+                        s2a = __ffma2_rn(make_float2(ww.x, ww.y),
+                                         make_float2(fmaxf(__uint_as_float(v[j]), 0.f),
+                                                     fmaxf(__uint_as_float(v[j + 1]), 0.f)), s2a);
+                        s2b = __ffma2_rn(make_float2(ww.z, ww.w),
+                                         make_float2(fmaxf(__uint_as_float(v[j + 2]), 0.f),
+                                                     fmaxf(__uint_as_float(v[j + 3]), 0.f)), s2b);
                     }
                 }
-                float uval = (part[0] + part[1]) + (part[2] + part[3]);
-                if (!kBeta)
-                    uval *= sc;
-                if (valid)
-                    out[static_cast<int64_t>(l) * p.L_out] = uval;
+                if ((i + 1) % CPL == 0) {
+                    float uval = (s2a.x + s2a.y) + (s2b.x + s2b.y);
+                    if (!kBeta)
+                        uval *= sc;
+                    if (valid)
+                        out[static_cast<int64_t>(i / CPL) * p.L_out] = uval;
+                    s2a = make_float2(0.f, 0.f);
+                    s2b = make_float2(0.f, 0.f);
+                }
+            };
+            uint32_t va[CH], vb[CH];
+            if (nchunks > 0)
+                tmem_ld_chunk(tbase, va);
+            for (int i = 0; i < nchunks; i += 2) {
+                tmem_wait_chunk(va);
+                if (i + 1 < nchunks)
+                    tmem_ld_chunk(tbase + static_cast<uint32_t>((i + 1) * CH), vb);
+                consume(i, va);
+                if (i + 1 < nchunks) {
+                    tmem_wait_chunk(vb);
+                    if (i + 2 < nchunks)
+                        tmem_ld_chunk(tbase + static_cast<uint32_t>((i + 2) * CH), va);
+                    consume(i + 1, vb);
+                }
             }
             tc_fence_before();
             __syncwarp();

@@ -1,4 +1,4 @@
-// topk.cu -- exact per-row top-k by radix select.
+// topk.cu -- exact per-row top-k.
 //
 // The TopK of eq. (8) in "LatentIndex: Cross-Layer Sharing with Layer-Specific
 // Selection for Sparse Attention" (summary page, Methodology): each layer
@@ -6,18 +6,29 @@
 //
 // Scores are mapped to order-preserving 32-bit keys (negative floats have all
 // bits flipped, non-negative ones the sign bit set; -0 is first folded to +0
-// so equal floats get equal keys).  The k-th largest key is found digit by
-// digit, most significant first (12 + 12 + 8 bits), from shared-memory
-// histograms; everything strictly above the threshold is emitted as soon as
-// its digit decides it, and among keys equal to the threshold the lowest
-// positions are taken (an in-order pass with block-wide ranks), which matches
-// a full sort by (score desc, position asc).
+// so equal floats get equal keys).  Selection is exact and matches a full
+// sort by (score desc, position asc): among keys equal to the k-th largest
+// the lowest positions are taken.
 //
-// One 1024-thread CTA per row.  The row is read twice from global memory
-// (histogram, then split); the elements in the threshold bin of the first
-// digit are kept in shared memory when they fit, so the later digits cost no
-// global traffic.  When they do not fit the row is re-read with a prefix
-// filter instead -- the kernel needs no global scratch memory.
+// One 1024-thread CTA per row, no global scratch memory:
+//  1. Sampled thresholds (rows of >= 8192 valid scores selecting at most about
+//     a quarter of them): 4096 stratified samples are histogrammed (12 + 12
+//     key bits) to find two keys whose sample ranks sit five standard
+//     deviations below (T_hi) and above (T_lo) k's expected rank.  One pass
+//     over the row, 32 elements per thread in registers with block-wide
+//     prefix sums for the output slots, emits every score >= T_hi (with
+//     overwhelming probability all of them belong to the top-k) and copies the
+//     band [T_lo, T_hi) into shared memory.  If the counts show that the k-th
+//     score is not inside the band (or the band does not fit), step 2 runs
+//     and overwrites every output slot.
+//  2. Exact radix fallback: a histogram of the top 12 key bits over the row,
+//     then a second pass that emits everything above the threshold bin and
+//     copies the bin into shared memory (or, if it does not fit, re-reads the
+//     row with a prefix filter for the lower digits).
+//  3. Among the shared-memory candidates, the remaining need is resolved digit
+//     by digit (12 + 12 + 8 bits) from shared-memory histograms; keys equal to
+//     the final threshold are ranked by position (in shared memory, or by an
+//     in-order pass over the row when there are very many of them).
 #include <atomic>
 #include <cstdint>
 
@@ -29,18 +40,25 @@ namespace {
 constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
 constexpr int kBins = 4096;
-constexpr int kCap = 12288;
+constexpr int kCap = 16384;        // (key, position) candidates in shared memory
+constexpr int kTieCap = 2048;      // ties ranked in shared memory
+constexpr int kSamples = 4096;     // 4 per thread
+constexpr int kMinSampledRow = 8192;
 
 struct TopkSmem {
     uint32_t hist[kBins];
     uint32_t ckey[kCap];
     int32_t cpos[kCap];
+    int32_t tpos[kTieCap];
     uint32_t warp_tot[kWarps];
     int emit_cnt;
     int cand_cnt;
+    int tie_cnt;
     int sel_bin;
     uint32_t sel_gt;
     int running;
+    uint32_t tot_sure;
+    uint32_t tot_band;
 };
 
 __device__ __forceinline__ uint32_t float_key(float x)
@@ -140,6 +158,166 @@ __device__ __forceinline__ void clear_hist(TopkSmem &sm)
         sm.hist[i] = 0u;
 }
 
+// Exclusive prefix sum over the 1024 threads; *total gets the block sum.
+__device__ __forceinline__ uint32_t block_excl_scan(TopkSmem &sm, uint32_t v, uint32_t *total)
+{
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    uint32_t x = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, x, off);
+        if (lane >= off)
+            x += y;
+    }
+    if (lane == 31)
+        sm.warp_tot[w] = x;
+    __syncthreads();
+    if (w == 0) {
+        uint32_t y = sm.warp_tot[lane];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const uint32_t z = __shfl_up_sync(0xffffffffu, y, off);
+            if (lane >= off)
+                y += z;
+        }
+        sm.warp_tot[lane] = y;
+    }
+    __syncthreads();
+    const uint32_t base = w > 0 ? sm.warp_tot[w - 1] : 0u;
+    *total = sm.warp_tot[kWarps - 1];
+    __syncthreads();
+    return base + x - v;
+}
+
+// Digit d of a key: d = 0 -> bits [31:20], 1 -> [19:8], 2 -> [7:0].
+__device__ __forceinline__ uint32_t digit(uint32_t key, int d)
+{
+    return d == 0 ? key >> 20 : (d == 1 ? (key >> 8) & 0xFFFu : key & 0xFFu);
+}
+__device__ __forceinline__ uint32_t digit_mask(int d)
+{
+    return d == 0 ? 0xFFF00000u : (d == 1 ? 0x000FFF00u : 0x000000FFu);
+}
+__device__ __forceinline__ int digit_shift(int d) { return d == 0 ? 20 : (d == 1 ? 8 : 0); }
+
+struct RowOut {
+    int32_t *idx;
+    float *val;
+    const int32_t *map;
+    int k;
+};
+
+__device__ __forceinline__ void emit(TopkSmem &sm, const RowOut &o, bool pred, int pos, uint32_t key)
+{
+    const int slot = reserve(&sm.emit_cnt, pred);
+    if (pred && slot < o.k) {
+        o.idx[slot] = o.map ? o.map[pos] : pos;
+        if (o.val)
+            o.val[slot] = key_float(key);
+    }
+}
+
+// In-order pass over the row: emit the `need` lowest positions whose key is K.
+__device__ void tie_pass_global(TopkSmem &sm, const RowOut &o, const float *src, int V, uint32_t K,
+                                uint32_t need)
+{
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    if (tid == 0)
+        sm.running = 0;
+    __syncthreads();
+    for (int base = 0; base < V; base += kThreads) {
+        const int pos = base + tid;
+        const bool pred = pos < V && float_key(src[pos]) == K;
+        const unsigned m = __ballot_sync(0xffffffffu, pred);
+        if (lane == 0)
+            sm.warp_tot[w] = __popc(m);
+        __syncthreads();
+        uint32_t before = 0, total = 0;
+        for (int w2 = 0; w2 < kWarps; ++w2) {
+            const uint32_t c = sm.warp_tot[w2];
+            before += w2 < w ? c : 0u;
+            total += c;
+        }
+        const uint32_t rank = static_cast<uint32_t>(sm.running) + before + __popc(m & ((1u << lane) - 1u));
+        emit(sm, o, pred && rank < need, pos, K);
+        __syncthreads();
+        if (tid == 0)
+            sm.running += static_cast<int>(total);
+        __syncthreads();
+        if (static_cast<uint32_t>(sm.running) >= need)
+            break;
+    }
+    __syncthreads();
+}
+
+// Select the `need` largest keys among the n shared-memory candidates and emit
+// them.  Returns true when done; false when the ties at the threshold are too
+// many to rank in shared memory (then *Kout / *need_out describe the tie pass
+// the caller runs over the row).
+__device__ bool select_candidates(TopkSmem &sm, const RowOut &o, int n, uint32_t need, uint32_t *Kout,
+                                  uint32_t *need_out)
+{
+    const int tid = threadIdx.x;
+    uint32_t prefix = 0, pmask = 0;
+    uint32_t last_count = 0;
+    for (int d = 0; d < 3; ++d) {
+        clear_hist(sm);
+        __syncthreads();
+        for (int i = tid; i < n; i += kThreads) {
+            const uint32_t key = sm.ckey[i];
+            if ((key & pmask) == prefix)
+                atomicAdd(&sm.hist[digit(key, d)], 1u);
+        }
+        __syncthreads();
+        int b;
+        uint32_t gt;
+        select_bin(sm, need, b, gt);
+        last_count = sm.hist[b];
+        for (int i = tid; i < n; i += kThreads) {
+            const uint32_t key = sm.ckey[i];
+            const bool pred = (key & pmask) == prefix && digit(key, d) > static_cast<uint32_t>(b);
+            emit(sm, o, pred, sm.cpos[i], key);
+        }
+        need -= gt;
+        prefix |= static_cast<uint32_t>(b) << digit_shift(d);
+        pmask |= digit_mask(d);
+        __syncthreads();
+    }
+    const uint32_t K = prefix;           // the k-th largest key; `need` of its copies remain
+    if (last_count == need) {
+        for (int i = tid; i < n; i += kThreads)
+            emit(sm, o, sm.ckey[i] == K, sm.cpos[i], K);
+        __syncthreads();
+        return true;
+    }
+    if (last_count > static_cast<uint32_t>(kTieCap)) {
+        *Kout = K;
+        *need_out = need;
+        return false;
+    }
+    // rank the ties by position inside shared memory
+    if (tid == 0)
+        sm.tie_cnt = 0;
+    __syncthreads();
+    for (int i = tid; i < n; i += kThreads) {
+        const bool pred = sm.ckey[i] == K;
+        const int slot = reserve(&sm.tie_cnt, pred);
+        if (pred)
+            sm.tpos[slot] = sm.cpos[i];
+    }
+    __syncthreads();
+    const int nt = sm.tie_cnt;
+    for (int i = tid; i < nt; i += kThreads) {
+        const int pi = sm.tpos[i];
+        int rank = 0;
+        for (int j = 0; j < nt; ++j)
+            rank += sm.tpos[j] < pi ? 1 : 0;
+        emit(sm, o, static_cast<uint32_t>(rank) < need, pi, K);
+    }
+    __syncthreads();
+    return true;
+}
+
 __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p)
 {
     extern __shared__ __align__(16) uint8_t smraw[];
@@ -155,164 +333,238 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p)
         }
         const int64_t grp = row / p.rows_per_group;
         const int64_t orow = grp * p.group_stride + row % p.rows_per_group + p.row_offset;
-        int32_t *oidx = p.idx + orow * p.k;
-        float *oval = p.vals ? p.vals + orow * p.k : nullptr;
-        const int32_t *map = p.map ? p.map + grp * p.map_stride : nullptr;
+        RowOut o;
+        o.idx = p.idx + orow * p.k;
+        o.val = p.vals ? p.vals + orow * p.k : nullptr;
+        o.map = p.map ? p.map + grp * p.map_stride : nullptr;
+        o.k = p.k;
         const int nsel = p.k < V ? p.k : V;
 
-        auto out_pos = [&](int pos) -> int32_t { return map ? map[pos] : pos; };
-        auto emit = [&](bool pred, int pos, uint32_t key) {
-            const int slot = reserve(&sm.emit_cnt, pred);
-            if (pred && slot < p.k) {
-                oidx[slot] = out_pos(pos);
-                if (oval)
-                    oval[slot] = key_float(key);
-            }
-        };
-
-        // padding
-        for (int j = nsel + tid; j < p.k; j += kThreads) {
-            oidx[j] = -1;
-            if (oval)
-                oval[j] = -__int_as_float(0x7f800000);
+        for (int j = nsel + tid; j < p.k; j += kThreads) {      // padding
+            o.idx[j] = -1;
+            if (o.val)
+                o.val[j] = -__int_as_float(0x7f800000);
         }
         if (nsel == V) {
             // everything valid is selected: positions in order
             for (int j = tid; j < V; j += kThreads) {
-                oidx[j] = out_pos(j);
-                if (oval)
-                    oval[j] = src[j];
+                o.idx[j] = o.map ? o.map[j] : j;
+                if (o.val)
+                    o.val[j] = src[j];
             }
             __syncthreads();
             continue;
         }
-
-        // ---- digit 1: bits [31:20] over the whole row
-        clear_hist(sm);
         if (tid == 0) {
             sm.emit_cnt = 0;
             sm.cand_cnt = 0;
-            sm.running = 0;
         }
-        __syncthreads();
-        for_row(src, V, [&](int, uint32_t key) { atomicAdd(&sm.hist[key >> 20], 1u); });
-        __syncthreads();
-        int b1;
-        uint32_t gt;
-        select_bin(sm, static_cast<uint32_t>(nsel), b1, gt);
-        uint32_t need = static_cast<uint32_t>(nsel) - gt;
-        const bool store1 = sm.hist[b1] <= static_cast<uint32_t>(kCap);
-        __syncthreads();
-        clear_hist(sm);
-        __syncthreads();
 
-        // ---- split on digit 1; histogram digit 2 (bits [19:8]) of the bin
-        for_row(src, V, [&](int pos, uint32_t key) {
-            const int d1 = static_cast<int>(key >> 20);
-            emit(d1 > b1, pos, key);
-            const bool in = d1 == b1;
-            if (in)
-                atomicAdd(&sm.hist[(key >> 8) & 0xFFFu], 1u);
-            if (store1) {
-                const int slot = reserve(&sm.cand_cnt, in);
-                if (in) {
-                    sm.ckey[slot] = key;
-                    sm.cpos[slot] = pos;
+        // ---------------------------------------------- 1. sampled thresholds
+        bool have_cands = false;
+        uint32_t need = static_cast<uint32_t>(nsel);
+        const float pk = static_cast<float>(nsel) / static_cast<float>(V);
+        const float sd = sqrtf(kSamples * pk * (1.f - pk));
+        const float rlo_f = kSamples * pk + 5.f * sd + 2.f;
+        const float rhi_f = kSamples * pk - 5.f * sd;
+        if (V >= kMinSampledRow && rlo_f < 0.3f * kSamples) {
+            clear_hist(sm);
+            __syncthreads();
+            for (int s2 = tid; s2 < kSamples; s2 += kThreads) {
+                const int lo = static_cast<int>(static_cast<int64_t>(s2) * V / kSamples);
+                const int hi = static_cast<int>(static_cast<int64_t>(s2 + 1) * V / kSamples);
+                const int pos = lo + static_cast<int>(((static_cast<uint32_t>(s2) * 2654435761u) >> 8) %
+                                                      static_cast<uint32_t>(hi - lo));
+                const uint32_t key = float_key(__ldg(src + pos));
+                sm.ckey[s2] = key;
+                atomicAdd(&sm.hist[key >> 20], 1u);
+            }
+            __syncthreads();
+            // sample key at a given (1-based, descending) rank, at 24-bit
+            // precision: the low boundary of its (digit0, digit1) bin.
+            // Expects the digit-0 histogram of the samples in sm.hist.
+            auto sample_bin = [&](uint32_t rank) -> uint32_t {
+                int c1, c2;
+                uint32_t g1, g2;
+                select_bin(sm, rank, c1, g1);
+                clear_hist(sm);
+                __syncthreads();
+                for (int s2 = tid; s2 < kSamples; s2 += kThreads) {
+                    const uint32_t key = sm.ckey[s2];
+                    if ((key >> 20) == static_cast<uint32_t>(c1))
+                        atomicAdd(&sm.hist[(key >> 8) & 0xFFFu], 1u);
+                }
+                __syncthreads();
+                select_bin(sm, rank - g1, c2, g2);
+                return (static_cast<uint32_t>(c1) << 20) | (static_cast<uint32_t>(c2) << 8);
+            };
+            const uint32_t T_lo = sample_bin(static_cast<uint32_t>(rlo_f));
+            uint32_t T_hi = 0xFFFFFFFFu;              // no "certain" scores
+            if (rhi_f >= 1.f) {
+                clear_hist(sm);
+                __syncthreads();
+                for (int s2 = tid; s2 < kSamples; s2 += kThreads)
+                    atomicAdd(&sm.hist[sm.ckey[s2] >> 20], 1u);
+                __syncthreads();
+                const uint32_t b = sample_bin(static_cast<uint32_t>(rhi_f));
+                if (b < 0xFFFFFF00u)
+                    T_hi = b + 0x100u;                // strictly above that bin
+            }
+            if (tid == 0) {
+                sm.tot_sure = 0;
+                sm.tot_band = 0;
+            }
+            __syncthreads();
+            // one pass, 32 scores per thread per 32K chunk held in registers
+            const bool al16 = (reinterpret_cast<uintptr_t>(src) & 15u) == 0;
+            for (int base = 0; base < V; base += 32 * kThreads) {
+                uint32_t key[32];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int pos = base + 4 * (tid + kThreads * i);
+                    if (al16 && pos + 3 < V) {
+                        const float4 v = __ldg(reinterpret_cast<const float4 *>(src + pos));
+                        key[4 * i] = float_key(v.x);
+                        key[4 * i + 1] = float_key(v.y);
+                        key[4 * i + 2] = float_key(v.z);
+                        key[4 * i + 3] = float_key(v.w);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            key[4 * i + j] = pos + j < V ? float_key(__ldg(src + pos + j)) : 0u;
+                    }
+                }
+                uint32_t ns = 0, nb = 0;
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const int pos = base + 4 * (tid + kThreads * (e / 4)) + (e & 3);
+                    const bool ok = pos < V;
+                    ns += (ok && key[e] >= T_hi) ? 1u : 0u;
+                    nb += (ok && key[e] >= T_lo && key[e] < T_hi) ? 1u : 0u;
+                }
+                uint32_t tot;
+                const uint32_t off = block_excl_scan(sm, (ns << 16) | nb, &tot);
+                uint32_t so = sm.tot_sure + (off >> 16);
+                uint32_t bo = sm.tot_band + (off & 0xFFFFu);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const int pos = base + 4 * (tid + kThreads * (e / 4)) + (e & 3);
+                    if (pos >= V)
+                        continue;
+                    if (key[e] >= T_hi) {
+                        if (so < static_cast<uint32_t>(nsel)) {
+                            o.idx[so] = o.map ? o.map[pos] : pos;
+                            if (o.val)
+                                o.val[so] = key_float(key[e]);
+                        }
+                        ++so;
+                    } else if (key[e] >= T_lo) {
+                        if (bo < static_cast<uint32_t>(kCap)) {
+                            sm.ckey[bo] = key[e];
+                            sm.cpos[bo] = pos;
+                        }
+                        ++bo;
+                    }
+                }
+                __syncthreads();
+                if (tid == 0) {
+                    sm.tot_sure += tot >> 16;
+                    sm.tot_band += tot & 0xFFFFu;
+                }
+                __syncthreads();
+            }
+            const uint32_t S = sm.tot_sure, Bn = sm.tot_band;
+            have_cands = S < need && S + Bn >= need && Bn <= static_cast<uint32_t>(kCap);
+            if (have_cands) {
+                need -= S;
+                if (tid == 0) {
+                    sm.emit_cnt = static_cast<int>(S);
+                    sm.cand_cnt = static_cast<int>(Bn);
                 }
             }
-        });
-        __syncthreads();
-        int b2;
-        select_bin(sm, need, b2, gt);
-        need -= gt;
-        const bool store2 = !store1 && sm.hist[b2] <= static_cast<uint32_t>(kCap);
-        __syncthreads();
-        clear_hist(sm);
-        __syncthreads();
+            __syncthreads();
+        }
 
-        // ---- split on digit 2; histogram digit 3 (bits [7:0])
-        const uint32_t pre1 = static_cast<uint32_t>(b1) << 20;
-        const uint32_t pre12 = pre1 | (static_cast<uint32_t>(b2) << 8);
-        auto step3 = [&](int pos, uint32_t key) {
-            const int d2 = static_cast<int>((key >> 8) & 0xFFFu);
-            emit(d2 > b2, pos, key);
-            const bool in = d2 == b2;
-            if (in)
-                atomicAdd(&sm.hist[key & 0xFFu], 1u);
-            if (store2) {
-                const int slot = reserve(&sm.cand_cnt, in);
-                if (in) {
-                    sm.ckey[slot] = key;
-                    sm.cpos[slot] = pos;
-                }
-            }
-        };
-        const int n1 = sm.cand_cnt;
-        if (store1) {
-            for (int i = tid; i < n1; i += kThreads)
-                step3(sm.cpos[i], sm.ckey[i]);
+        int n = 0;
+        bool stored = have_cands;
+        int b1 = 0;
+        if (have_cands) {
+            n = sm.cand_cnt;
         } else {
+            // ------------------------------------------ 2. exact radix fallback
+            clear_hist(sm);
+            if (tid == 0) {
+                sm.emit_cnt = 0;
+                sm.cand_cnt = 0;
+            }
+            __syncthreads();
+            for_row(src, V, [&](int, uint32_t key) { atomicAdd(&sm.hist[key >> 20], 1u); });
+            __syncthreads();
+            uint32_t gt;
+            select_bin(sm, need, b1, gt);
+            stored = sm.hist[b1] <= static_cast<uint32_t>(kCap);
+            __syncthreads();
             for_row(src, V, [&](int pos, uint32_t key) {
+                const uint32_t d1 = key >> 20;
+                emit(sm, o, d1 > static_cast<uint32_t>(b1), pos, key);
+                if (stored) {
+                    const bool in = d1 == static_cast<uint32_t>(b1);
+                    const int slot = reserve(&sm.cand_cnt, in);
+                    if (in) {
+                        sm.ckey[slot] = key;
+                        sm.cpos[slot] = pos;
+                    }
+                }
+            });
+            __syncthreads();
+            need -= gt;
+            n = sm.cand_cnt;
+            __syncthreads();
+        }
+
+        if (stored) {
+            // --------------------------------- 3. select among the candidates
+            uint32_t K = 0, need_eq = 0;
+            if (!select_candidates(sm, o, n, need, &K, &need_eq))
+                tie_pass_global(sm, o, src, V, K, need_eq);
+        } else {
+            // the threshold bin does not fit: lower digits by re-reading the row
+            const uint32_t pre1 = static_cast<uint32_t>(b1) << 20;
+            clear_hist(sm);
+            __syncthreads();
+            for_row(src, V, [&](int, uint32_t key) {
                 if ((key & 0xFFF00000u) == pre1)
-                    step3(pos, key);
+                    atomicAdd(&sm.hist[(key >> 8) & 0xFFFu], 1u);
             });
-        }
-        __syncthreads();
-        int b3;
-        select_bin(sm, need, b3, gt);
-        need -= gt;                                  // ties needed at the threshold
-        const uint32_t K = pre12 | static_cast<uint32_t>(b3);
-        const bool take_all_ties = sm.hist[b3] == need;
-        const int n2 = sm.cand_cnt;
-        __syncthreads();
-
-        // ---- emit keys above the threshold (and the ties when all are taken)
-        auto step4 = [&](int pos, uint32_t key) {
-            emit(key > K || (take_all_ties && key == K), pos, key);
-        };
-        if (store1) {
-            for (int i = tid; i < n1; i += kThreads) {
-                const uint32_t key = sm.ckey[i];
-                if ((key & 0xFFFFFF00u) == pre12)
-                    step4(sm.cpos[i], key);
-            }
-        } else if (store2) {
-            for (int i = tid; i < n2; i += kThreads)
-                step4(sm.cpos[i], sm.ckey[i]);
-        } else {
+            __syncthreads();
+            int b2;
+            uint32_t gt;
+            select_bin(sm, need, b2, gt);
+            need -= gt;
+            const uint32_t pre12 = pre1 | (static_cast<uint32_t>(b2) << 8);
+            clear_hist(sm);
+            __syncthreads();
             for_row(src, V, [&](int pos, uint32_t key) {
-                if ((key & 0xFFFFFF00u) == pre12)
-                    step4(pos, key);
+                const bool in = (key & 0xFFF00000u) == pre1;
+                const uint32_t d2 = (key >> 8) & 0xFFFu;
+                emit(sm, o, in && d2 > static_cast<uint32_t>(b2), pos, key);
+                if (in && d2 == static_cast<uint32_t>(b2))
+                    atomicAdd(&sm.hist[key & 0xFFu], 1u);
             });
-        }
-        __syncthreads();
-
-        // ---- ties: the `need` lowest positions whose key equals K, in order
-        if (!take_all_ties) {
-            for (int base = 0; base < V; base += kThreads) {
-                const int pos = base + tid;
-                const bool pred = pos < V && float_key(src[pos]) == K;
-                const unsigned m = __ballot_sync(0xffffffffu, pred);
-                const int lane = tid & 31, w = tid >> 5;
-                if (lane == 0)
-                    sm.warp_tot[w] = __popc(m);
-                __syncthreads();
-                uint32_t before = 0, total = 0;
-                for (int w2 = 0; w2 < kWarps; ++w2) {
-                    const uint32_t c = sm.warp_tot[w2];
-                    before += w2 < w ? c : 0u;
-                    total += c;
-                }
-                const uint32_t rank = static_cast<uint32_t>(sm.running) + before +
-                                      __popc(m & ((1u << lane) - 1u));
-                emit(pred && rank < need, pos, K);
-                __syncthreads();
-                if (tid == 0)
-                    sm.running += static_cast<int>(total);
-                __syncthreads();
-                if (static_cast<uint32_t>(sm.running) >= need)
-                    break;
-            }
+            __syncthreads();
+            int b3;
+            select_bin(sm, need, b3, gt);
+            need -= gt;
+            const uint32_t K = pre12 | static_cast<uint32_t>(b3);
+            const bool all_ties = sm.hist[b3] == need;
+            __syncthreads();
+            for_row(src, V, [&](int pos, uint32_t key) {
+                const bool in = (key & 0xFFFFFF00u) == pre12;
+                emit(sm, o, in && (key > K || (all_ties && key == K)), pos, key);
+            });
+            __syncthreads();
+            if (!all_ties)
+                tie_pass_global(sm, o, src, V, K, need);
         }
         __syncthreads();
     }

@@ -27,9 +27,8 @@ def declared_functions():
 
 
 @pytest.fixture(scope="module")
-def L():
-    import shared_latent_key_cache_b300 as m
-    return m.lib()
+def L(li):
+    return li.lib()
 
 
 def test_header_declares_the_boundary():
@@ -44,7 +43,7 @@ def test_library_exports_every_declared_symbol(L):
         assert hasattr(L, n), f"{n} declared in li.h but not exported"
 
 
-def test_exports_are_c_symbols():
+def test_exports_are_c_symbols(li):
     so = os.path.join(ROOT, "shared_latent_key_cache_b300", "libli_b300.so")
     lib = ctypes.CDLL(so)
     for n in declared_functions():

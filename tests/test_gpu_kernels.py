@@ -306,3 +306,64 @@ def test_hs_budget_equal_k_gives_candidates(li, orc):
     for b in range(2):
         for l in range(w.G):
             assert set(gi[b, l].tolist()) == set(c[b].tolist())
+
+
+@pytest.mark.parametrize("d,r", [(40, 64), (36, 100), (128, 256)])
+def test_absorb_odd_widths(li, orc, d, r):
+    """Key widths that are not multiples of the 32-wide staging chunk (d = 40) or
+    of the 16-byte load (d = 36), and output widths that are not multiples of 4."""
+    g = torch.Generator().manual_seed(d + r)
+    q = torch.randn(2, 3, 2, 16, d, generator=g).to(torch.bfloat16)
+    D = (torch.randn(2, r, d, generator=g) / r ** 0.5).to(torch.bfloat16)
+    o = orc.absorb(q, D)
+    for abs_dtype in ("f32", "bf16", "fp8"):
+        q_abs, scale = li.absorb_queries(q.to(DEV), D.to(DEV), abs_dtype)
+        _sync_ok(li)
+        if abs_dtype == "fp8":
+            gv = orc.decode_rows(q_abs.cpu(), scale.cpu())
+            s = scale.cpu().numpy()[..., None]
+            tol = 2.0 ** -4 * np.abs(o) + s * 2.0 ** -10 + 1e-5 * np.abs(o).max()
+        elif abs_dtype == "bf16":
+            gv = q_abs.float().cpu().double().numpy()
+            tol = 2.0 ** -8 * np.abs(o) + 1e-6 * np.abs(o).max()
+        else:
+            gv = q_abs.cpu().double().numpy()
+            tol = 1e-5 * np.abs(o) + 1e-6 * np.abs(o).max()
+        assert (np.abs(gv - o) <= tol).all(), abs_dtype
+
+
+def test_topk_long_rows_with_heavy_ties(li, orc):
+    """Long rows of a few distinct values: the sampled thresholds see thousands of
+    ties, so the shared-memory tie ranking and the in-order tie pass both run."""
+    g = torch.Generator().manual_seed(15)
+    s = torch.randint(0, 7, (4, 50000), generator=g).float()
+    s[3] = torch.where(torch.rand(50000, generator=g) < 0.01, 9.0, 1.0)   # 1% on top, rest tied
+    for k in (1, 300, 2048, 7000, 12000):
+        gi, _ = _topk_gpu(li, s, k)
+        oi, _ = orc.topk(s.double().numpy(), k)
+        exact_sets_equal(gi, oi)
+
+
+def test_topk_many_long_rows_valid_len(li, orc):
+    """Prefill-shaped rows: long, with per-row valid lengths around the causal limit."""
+    g = torch.Generator().manual_seed(16)
+    rows, L = 24, 131072
+    s = torch.randn(rows, L, generator=g) * 3 + 20
+    vl = torch.randint(L - 5000, L + 1, (rows,), generator=g, dtype=torch.int32)
+    vl[0] = 8191
+    vl[1] = 8192
+    gi, _ = _topk_gpu(li, s, 2048, vl)
+    oi, _ = orc.topk(s.double().numpy(), 2048, valid_len=vl.numpy())
+    exact_sets_equal(gi, oi)
+
+
+def test_topk_unaligned_rows(li, orc):
+    """Row starts that are not 16-byte aligned take the scalar load paths."""
+    g = torch.Generator().manual_seed(17)
+    base = torch.randn(5 * 30001 + 16, generator=g).to(DEV)
+    s = base[4:4 + 5 * 30001].view(5, 30001)     # 16-byte aligned start, odd row length
+    idx = torch.empty(5, 1000, dtype=torch.int32, device=DEV)
+    st = li.li_topk(s, 1000, idx)
+    assert st == 0 and li.li_device_status() == 0
+    oi, _ = orc.topk(s.cpu().double().numpy(), 1000)
+    exact_sets_equal(idx.cpu().numpy(), oi)
