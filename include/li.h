@@ -150,6 +150,34 @@ int li_hs_select(const void *latent, int lat_t, const float *lat_scale,
                  int32_t *cand, int32_t *idx, void *ws, size_t ws_bytes, void *stream);
 
 /*
+ * Hierarchical selection without a caller workspace.  The paper has no
+ * counterpart: this entry point exists for callers that cannot allocate device
+ * memory where they run the indexer -- for example a plugin inside a serving
+ * engine whose device memory is all owned by the engine's pool, or a decode
+ * loop that must not call cudaMalloc (it can synchronise the device).
+ *
+ * Same arguments, outputs and results as li_hs_select, minus ws / ws_bytes.
+ * The scratch is a fixed 8 MiB device array inside this library (8,388,608
+ * bytes; every GPU that loads the library holds it until the process exits).
+ * Sizes whose li_hs_workspace_size(B, G, L, m, k) exceeds 8 MiB are rejected
+ * with LI_ERR_WORKSPACE before anything runs (B = 8, L = 131072, m = 8192,
+ * G = 4 needs 5 MiB).  The call allocates nothing.
+ *  - The first call on a device, made with that device current, looks up the
+ *    array's device address (cudaGetSymbolAddress) and caches it; make that
+ *    first call before any stream capture.
+ *  - All calls on a device share the one array and leave their contents in
+ *    it; nothing in it has to start at zero (every value a call reads was
+ *    written earlier in the same call).  Calls that may overlap on the GPU
+ *    (different streams without ordering between them) race on the array:
+ *    order them, or use li_hs_select with separate workspaces.
+ */
+int li_hs_select_noalloc(const void *latent, int lat_t, const float *lat_scale,
+                         const void *q_abs, int abs_t, const float *q_abs_scale,
+                         const float *w, const float *beta,
+                         int B, int G, int H, int r, int L, int m, int k,
+                         int32_t *cand, int32_t *idx, void *stream);
+
+/*
  * Native per-layer DSA lightning indexer over one layer's own key cache, the
  * baseline LatentIndex replaces (explainer page: "DSA lightning indexer",
  * "Indexer key cache" of 132 B per token per layer = 128 fp8 values + one

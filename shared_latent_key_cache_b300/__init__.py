@@ -22,7 +22,8 @@ import torch
 __all__ = [
     "LI_F32", "LI_BF16", "LI_FP8_E4M3", "LiError", "lib", "library_path",
     "li_version", "li_status_string", "li_absorb_queries", "li_score_group", "li_topk",
-    "li_hs_workspace_size", "li_hs_select", "li_native_score", "li_device_status",
+    "li_hs_workspace_size", "li_hs_select", "li_hs_select_noalloc", "li_native_score",
+    "li_device_status",
     "absorb_queries", "score_group", "topk", "hs_select", "native_score", "device_status",
 ]
 
@@ -56,9 +57,10 @@ def _load():
     L.li_hs_workspace_size.restype = S
     L.li_hs_select.argtypes = [P, I, P, P, I, P, P, P, I, I, I, I, I, I, I, P, P, P, S, P]
     L.li_native_score.argtypes = [P, I, P, P, I, P, P, I, I, I, I, P, P]
+    L.li_hs_select_noalloc.argtypes = [P, I, P, P, I, P, P, P, I, I, I, I, I, I, I, P, P, P]
     L.li_device_status.argtypes = [P]
     for f in ("li_absorb_queries", "li_score_group", "li_topk", "li_hs_select",
-              "li_native_score", "li_device_status"):
+              "li_native_score", "li_device_status", "li_hs_select_noalloc"):
         getattr(L, f).restype = I
     return L
 
@@ -158,6 +160,19 @@ def li_hs_select(latent, lat_scale, q_abs, q_abs_scale, w, m: int, k: int, cand,
         _ptr(latent), _dtype_code(latent), _ptr(lat_scale), _ptr(q_abs), _dtype_code(q_abs),
         _ptr(q_abs_scale), _ptr(w), _ptr(beta), B, G, H, r, L, m, k, _ptr(cand), _ptr(idx),
         _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
+
+
+def li_hs_select_noalloc(latent, lat_scale, q_abs, q_abs_scale, w, m: int, k: int, cand, idx,
+                         beta=None, stream=None) -> int:
+    """As li_hs_select, with the library's built-in 8 MiB scratch instead of a
+    caller workspace (for callers that cannot allocate device memory)."""
+    B, L, r = latent.shape
+    _, T, G, H, _ = q_abs.shape
+    assert T == 1
+    return _lib.li_hs_select_noalloc(
+        _ptr(latent), _dtype_code(latent), _ptr(lat_scale), _ptr(q_abs), _dtype_code(q_abs),
+        _ptr(q_abs_scale), _ptr(w), _ptr(beta), B, G, H, r, L, m, k, _ptr(cand), _ptr(idx),
+        _stream(stream))
 
 
 def li_native_score(keys, key_scale, q, q_scale, w, scores, stream=None) -> int:
