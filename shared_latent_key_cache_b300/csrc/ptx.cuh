@@ -67,26 +67,43 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
+// As mbar_try_wait, but a thread whose phase is not complete yet is suspended
+// in hardware until it completes or about `hint_ns` nanoseconds pass, instead
+// of returning at once: waiting threads issue (almost) no instructions, so
+// they do not take issue slots from the warps that do the work.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t hint_ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Bounded wait for the phase with the given parity to complete.
 // Returns false (after latching the timeout) when `limit_ns` ran out or when
-// another role of the CTA already aborted (*abort != 0).
+// another role of the CTA already aborted (*abort != 0).  Each attempt
+// suspends the thread for up to 0.2 ms, so the abort flag is looked at least
+// every 0.2 ms and the clock at most a few thousand times per wait.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
                                           int *status, uint64_t limit_ns)
 {
     if (mbar_try_wait(bar, parity))
         return true;
-    uint64_t t0 = globaltimer_ns();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity))
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity, 200000u))
             return true;
-        if ((it & 63u) == 0u) {
-            if (*abort)
-                return false;
-            if (globaltimer_ns() - t0 > limit_ns) {
-                *abort = 1;
-                atomicCAS(status, 0, -6 /* LI_ERR_TIMEOUT */);
-                return false;
-            }
+        if (*abort)
+            return false;
+        if (globaltimer_ns() - t0 > limit_ns) {
+            *abort = 1;
+            atomicCAS(status, 0, -6 /* LI_ERR_TIMEOUT */);
+            return false;
         }
     }
 }
@@ -116,6 +133,51 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, u
         " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
         : "memory");
+}
+
+// 3D tile load with an L2 cache policy (from make_l2_policy).
+__device__ __forceinline__ void tma_load_3d_hint(void *dst, const CUtensorMap *map, uint64_t *bar,
+                                                 int x, int y, int z, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z), "l"(policy)
+        : "memory");
+}
+
+// L2 policy for data read once (evict first) or re-read by other CTAs (normal).
+__device__ __forceinline__ uint64_t make_l2_policy(bool evict_first)
+{
+    uint64_t pol;
+    if (evict_first)
+        asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    else
+        asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// ------------------------------------------------------------------ cp.async
+
+// 16-byte global -> shared copy; src_bytes = 0 writes 16 zero bytes and reads
+// nothing.
+__device__ __forceinline__ void cp_async_16(uint32_t dst_smem, const void *src, uint32_t src_bytes)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst_smem), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit()
+{
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// Wait until at most N of this thread's committed cp.async groups are pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group()
+{
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // Make this thread's generic-proxy shared-memory writes visible to the async

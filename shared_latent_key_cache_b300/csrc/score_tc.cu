@@ -17,21 +17,27 @@
 // the inner loop (w s_q is precomputed per query, s_c applied once per token).
 // With beta the scales are applied before the ReLU.
 //
-// Roles of the 384 threads (one persistent CTA per SM, static contiguous
-// split of the (query, 128-token tile) work units):
-//   warp 0      TMA producer: latent tiles -> smem ring (and the query
-//               operand whenever the work unit's query changes)
-//   warp 1      TMEM allocation and the single-thread MMA issuer
-//   warps 2-3   gather mode only: with warp 0, copy gathered latent rows
-//               into the swizzled smem layout (HS followers rescoring the
-//               anchor's candidates)
-//   warps 4-11  epilogue, two warps per TMEM lane quarter (warp % 4), each
-//               taking half of the layers: TMEM -> registers 32 columns at a
-//               time (the next chunk's load in flight while the current one
-//               is reduced), ReLU, weighted head sums with packed fp32 FMA,
-//               per-token scale, one coalesced score store per layer
-// The two TMEM accumulators are double-buffered so the epilogue of tile i
-// overlaps the MMAs of tile i+1 and the loads of the tiles after it.
+// Roles (one persistent CTA per SM, static contiguous split of the
+// (query row, 128-token tile) work units; every role walks the same units):
+//   warp 0          TMEM allocation and the single-thread MMA issuer
+//   warp 1          scan mode: TMA producer of the latent tiles (smem ring) and
+//                   of the absorbed-query operand (double-buffered when it
+//                   fits, so the next query's operand loads under the current
+//                   query's tiles)
+//   warps 1-4       gather mode (HS followers rescoring the anchor's
+//                   candidates): one thread per tile row copies its gathered
+//                   latent row with 16-byte cp.async into the swizzled layout
+//                   TMA would write, several tiles in flight per thread
+//   16 warps        epilogue, four per TMEM lane quarter (warp % 4), each
+//                   owning 64 (or H when H > 64) accumulator columns, i.e. one
+//                   layer at H = 64: both 32-column TMEM loads in flight, the
+//                   accumulator released as soon as they land, then ReLU,
+//                   weighted head sums with packed fp32 FMA, per-token scale
+//                   (prefetched one tile ahead) and one coalesced store per
+//                   layer
+// The two TMEM accumulators (2 x 256 columns) are double-buffered so the
+// epilogue of tile i overlaps the MMAs of tile i+1 and the loads of the tiles
+// after it.
 //
 // Operand layouts: K-major, split in 64-element K chunks; bf16 chunks are
 // 128-byte rows (128B swizzle), fp8 chunks 64-byte rows (64B swizzle); an
@@ -48,32 +54,48 @@
 namespace li {
 namespace {
 
-constexpr int kThreads = 384;
-constexpr int kEpiWarps = 8;
 constexpr int kTileM = 128;
 constexpr int kChunkElems = 64;
 constexpr int kMaxDev = 64;
-constexpr int kSmemBudget = 200 * 1024;
+constexpr int kEpiWarps = 16;
+constexpr int kTmemCols = 512;          // two accumulators of 256 columns
+constexpr int kAccStride = 256;
+constexpr int kConstCap = 1024;         // active epilogue warps x columns per warp
+constexpr int kSmemLimit = 227 * 1024;
+
+template <bool kGather>
+struct Roles {
+    static constexpr int kMmaWarp = 0;
+    static constexpr int kProdWarp0 = 1;
+    static constexpr int kProdWarps = kGather ? 2 : 1;
+    static constexpr int kEpiWarp0 = 1 + kProdWarps;
+    static constexpr int kThreads = 32 * (1 + kProdWarps + kEpiWarps);
+};
 
 struct TcConfig {
     int N;              // Gs * H
     int nchunk;         // r / 64
-    int stages;
+    int stages;         // latent tile ring depth
+    int nbuf;           // query-operand buffers (1 or 2)
     int a_chunk_bytes;  // 128 * 64 * esz
     int b_chunk_bytes;  // N * 64 * esz
     int a_stage_bytes;
+    int b_bytes;        // one query operand
+    int b_buf_stride;   // 1024-aligned
     int off_a;          // byte offsets from the 1024-aligned base
     int off_bar;
     int off_misc;
-    int tmem_cols;
-    int acc_stride;     // TMEM column distance of the two accumulators
+    int cw;             // accumulator columns per epilogue warp
+    int nepi;           // epilogue warps with columns
+    int gdepth;         // gather mode: tiles in flight per copying thread
     int NT;             // tiles per query row
     int64_t U;          // total work units
 };
 
 struct __align__(8) Bars {
-    uint64_t b_full, b_empty, done;
+    uint64_t b_full[2], b_empty[2];
     uint64_t tmem_full[2], tmem_empty[2];
+    uint64_t done;
 };
 
 struct Misc {
@@ -81,68 +103,112 @@ struct Misc {
     int abort;
     int pad[2];
     // per-epilogue-warp copies of the current query's head constants for the
-    // warp's layers (<= 128 columns), so no cross-warp barrier is needed when
-    // the query changes
-    float wq[kEpiWarps][128];
-    float sq[kEpiWarps][128];
-    float bq[kEpiWarps][128];
+    // warp's columns, so that no cross-warp barrier is needed when the query
+    // changes
+    float wq[kConstCap];
+    float sq[kConstCap];
+    float bq[kConstCap];
 };
 
-// One lane polls, the whole warp gets the (uniform) outcome.
+// The whole (converged) warp waits; the outcome is made warp-uniform, so that
+// a warp never splits on a wait that ran out.
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
                                           int *status)
 {
-    bool ok = true;
-    if ((threadIdx.x & 31) == 0)
-        ok = mbar_wait(bar, parity, abort, status, kWaitLimitNs);
-    return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    const bool ok = mbar_wait(bar, parity, abort, status, kWaitLimitNs);
+    return __all_sync(0xffffffffu, ok);
 }
 
-// Walks a CTA's contiguous range of (query row bt, 128-token tile) work units
-// without a 64-bit division per unit.
-struct UnitIter {
-    int64_t bt;
-    int tile;
-    int NT;
-    __device__ __forceinline__ UnitIter(int64_t u, int nt) : bt(u / nt), tile(static_cast<int>(u % nt)), NT(nt) {}
-    __device__ __forceinline__ void next()
-    {
-        if (++tile == NT) {
-            tile = 0;
-            ++bt;
-        }
-    }
-};
-
-__device__ __forceinline__ int seq_of(int64_t bt, int T)
+__device__ __forceinline__ int seq_of(int bt, int T)
 {
-    return T == 1 ? static_cast<int>(bt) : static_cast<int>(bt / T);
+    return T == 1 ? bt : bt / T;
 }
 
 template <bool kGather>
-__device__ __forceinline__ int unit_valid_len(const ScoreParams &p, int64_t bt)
+__device__ __forceinline__ int unit_valid_len(const ScoreParams &p, int bt)
 {
     if (kGather)
         return p.n_gather;
     if (p.q_pos == nullptr)
         return p.L_lat;
-    int t = static_cast<int>(bt % p.T);
-    int lim = p.q_pos[t] + 1;
+    const int t = bt % p.T;
+    const int lim = p.q_pos[t] + 1;
     return lim < p.L_lat ? lim : p.L_lat;
 }
 
+// Walks a CTA's contiguous range of (query row bt, 128-token tile) work units,
+// skipping tiles that lie entirely past the row's valid length (causal
+// prefill), without a division per unit.  `left` counts the units of the
+// range from the current one on.
+template <bool kGather>
+struct Walk {
+    int left, bt, tile, Lv;
+
+    __device__ __forceinline__ void init(const ScoreParams &p, int64_t ub, int64_t ue, int NT)
+    {
+        left = static_cast<int>(ue - ub);
+        bt = static_cast<int>(ub / NT);
+        tile = static_cast<int>(ub % NT);
+        Lv = left > 0 ? unit_valid_len<kGather>(p, bt) : 0;
+        settle(p, NT);
+    }
+    __device__ __forceinline__ void settle(const ScoreParams &p, int NT)
+    {
+        while (left > 0 && tile * kTileM >= Lv) {
+            left -= NT - tile;
+            ++bt;
+            tile = 0;
+            if (left > 0)
+                Lv = unit_valid_len<kGather>(p, bt);
+        }
+    }
+    __device__ __forceinline__ bool ok() const { return left > 0; }
+    __device__ __forceinline__ void next(const ScoreParams &p, int NT)
+    {
+        --left;
+        if (++tile == NT) {
+            tile = 0;
+            ++bt;
+            if (left > 0)
+                Lv = unit_valid_len<kGather>(p, bt);
+        }
+        settle(p, NT);
+    }
+};
+
+// Ties the registers of a finished tcgen05.ld to the preceding wait::ld (which
+// covers every outstanding load of the thread) without another wait.
+__device__ __forceinline__ void tmem_regs_ready(uint32_t (&v)[32])
+{
+    asm volatile(""
+                 : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]), "+r"(v[6]), "+r"(v[7]), "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]), "+r"(v[12]), "+r"(v[13]), "+r"(v[14]), "+r"(v[15]), "+r"(v[16]), "+r"(v[17]), "+r"(v[18]), "+r"(v[19]), "+r"(v[20]), "+r"(v[21]), "+r"(v[22]), "+r"(v[23]), "+r"(v[24]), "+r"(v[25]), "+r"(v[26]), "+r"(v[27]), "+r"(v[28]), "+r"(v[29]), "+r"(v[30]), "+r"(v[31])
+                 :
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_depth(int depth)
+{
+    if (depth <= 1)
+        cp_async_wait_group<1>();
+    else if (depth == 2)
+        cp_async_wait_group<2>();
+    else
+        cp_async_wait_group<3>();
+}
+
 template <bool kFP8, bool kGather, bool kBeta, int kH>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Roles<kGather>::kThreads, 1)
     score_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const ScoreParams p, const TcConfig c)
 {
+    using R = Roles<kGather>;
     constexpr int kEsz = kFP8 ? 1 : 2;
     constexpr int kKStep = 32 / kEsz;              // elements per MMA K step (32 bytes)
     constexpr int kStepsPerChunk = kChunkElems / kKStep;
     constexpr uint32_t kSwz = kFP8 ? 4u : 2u;      // 64B : 128B swizzle
     constexpr uint32_t kSbo = 8u * kChunkElems * kEsz;
-    constexpr int kPiece = 16;                     // bytes per gather copy
-    constexpr int kPiecesPerChunk = kChunkElems * kEsz / kPiece;
+    constexpr int kRowChunkBytes = kChunkElems * kEsz;
+    constexpr int kPiecesPerChunk = kRowChunkBytes / 16;
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -163,21 +229,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < c.stages; ++s) {
-            mbar_init(&full[s], kGather ? 3u : 1u);
+            mbar_init(&full[s], kGather ? static_cast<uint32_t>(R::kProdWarps) : 1u);
             mbar_init(&empty[s], 1u);
         }
-        mbar_init(&bars->b_full, 1u);
-        mbar_init(&bars->b_empty, 1u);
-        mbar_init(&bars->done, 1u);
         for (int a = 0; a < 2; ++a) {
+            mbar_init(&bars->b_full[a], 1u);
+            mbar_init(&bars->b_empty[a], 1u);
             mbar_init(&bars->tmem_full[a], 1u);
-            mbar_init(&bars->tmem_empty[a], static_cast<uint32_t>(kEpiWarps));
+            mbar_init(&bars->tmem_empty[a], static_cast<uint32_t>(c.nepi));
         }
+        mbar_init(&bars->done, 1u);
         misc->abort = 0;
         mbar_fence_init();
     }
-    if (warp == 1) {
-        tmem_alloc(&misc->tmem_base, static_cast<uint32_t>(c.tmem_cols));
+    if (warp == R::kMmaWarp) {
+        tmem_alloc(&misc->tmem_base, static_cast<uint32_t>(kTmemCols));
         tmem_relinquish();
     }
     tc_fence_before();
@@ -185,175 +251,64 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = misc->tmem_base;
 
-    if (!kGather && warp == 0) {
-        // ------------------------------------------------- TMA producer (1 thread)
+    // Issues the query operand of row bt into buffer (nb % nbuf); returns false
+    // on abort.  Called by a whole warp; lane 0 issues the copies.
+    auto load_query_operand = [&](int bt, int nb) -> bool {
+        const int bb = nb % c.nbuf;
+        const int use = nb / c.nbuf;
+        if (use > 0 &&
+            !warp_wait(&bars->b_empty[bb], static_cast<uint32_t>(use - 1) & 1u, abort_flag, p.status))
+            return false;
         if (lane == 0) {
-            tma_prefetch_desc(&tmA);
-            tma_prefetch_desc(&tmB);
-            int stage = 0;
-            uint32_t phase = 0;
-            int64_t cur_bt = -1;
-            int nb = 0;
-            uint32_t last_par[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-            bool used[8] = {false, false, false, false, false, false, false, false};
-            UnitIter it(u_begin, c.NT);
-            for (int64_t u = u_begin; u < u_end; ++u, it.next()) {
-                const int64_t bt = it.bt;
-                const int tile = it.tile;
-                if (tile * kTileM >= unit_valid_len<kGather>(p, bt))
-                    continue;
-                if (bt != cur_bt) {
-                    if (nb > 0 && !mbar_wait(&bars->b_empty, (nb - 1) & 1, abort_flag, p.status,
-                                             kWaitLimitNs))
-                        break;
-                    mbar_arrive_expect_tx(&bars->b_full,
-                                          static_cast<uint32_t>(c.nchunk * c.b_chunk_bytes));
-                    const int row0 = static_cast<int>((bt * p.Gtot + p.g0) * p.H);
-                    for (int ch = 0; ch < c.nchunk; ++ch)
-                        tma_load_2d(smB + ch * c.b_chunk_bytes, &tmB, &bars->b_full,
-                                    ch * kChunkElems, row0);
-                    cur_bt = bt;
-                    ++nb;
-                }
-                if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status, kWaitLimitNs))
-                    break;
-                uint8_t *dstA = smA + stage * c.a_stage_bytes;
-                mbar_arrive_expect_tx(&full[stage], static_cast<uint32_t>(c.a_stage_bytes));
-                const int b = seq_of(bt, p.T);
-                for (int ch = 0; ch < c.nchunk; ++ch)
-                    tma_load_3d(dstA + ch * c.a_chunk_bytes, &tmA, &full[stage], ch * kChunkElems,
-                                tile * kTileM, b);
-                used[stage] = true;
-                last_par[stage] = phase;
-                if (++stage == c.stages) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
-            }
-            // Never leave the CTA with copies in flight: wait (bounded) for the
-            // last load issued into each stage and for the last query operand.
-            for (int s2 = 0; s2 < c.stages; ++s2)
-                if (used[s2])
-                    mbar_wait(&full[s2], last_par[s2], abort_flag, p.status, kWaitLimitNs);
-            if (nb > 0)
-                mbar_wait(&bars->b_full, (nb - 1) & 1, abort_flag, p.status, kWaitLimitNs);
+            mbar_arrive_expect_tx(&bars->b_full[bb], static_cast<uint32_t>(c.b_bytes));
+            const int row0 = (bt * p.Gtot + p.g0) * p.H;
+            uint8_t *dst = smB + bb * c.b_buf_stride;
+            for (int ch = 0; ch < c.nchunk; ++ch)
+                tma_load_2d(dst + ch * c.b_chunk_bytes, &tmB, &bars->b_full[bb], ch * kChunkElems, row0);
         }
         __syncwarp();
-    } else if (kGather && (warp == 0 || warp == 2 || warp == 3)) {
-        // ------------------------------- gather producer (3 warps, 96 threads)
-        // Copies the rows of the gathered token indices into the same swizzled
-        // K-major layout TMA would write; warp 0 lane 0 also loads the query
-        // operand by TMA.  All decisions are warp-uniform.
-        const int pid = (warp == 0 ? 0 : warp - 1) * 32 + lane;
-        if (warp == 0 && lane == 0)
-            tma_prefetch_desc(&tmB);
+        return true;
+    };
+    // Never leave the CTA with query-operand copies in flight.
+    auto drain_query_operand = [&](int nb) {
+        for (int j = nb - 1; j >= 0 && j >= nb - c.nbuf; --j)
+            mbar_wait(&bars->b_full[j % c.nbuf], static_cast<uint32_t>(j / c.nbuf) & 1u, abort_flag,
+                      p.status, kWaitLimitNs);
+    };
+
+    if (warp == R::kMmaWarp) {
+        // ---------------------------------------------------------- MMA issuer
+        // The warp walks the units together; lane 0 issues the MMAs and commits.
+        const uint32_t idesc = umma_idesc(kFP8, kTileM, c.N);
+        const uint32_t a_base = smem_u32(smA);
+        const uint32_t b_base0 = smem_u32(smB);
         int stage = 0;
         uint32_t phase = 0;
-        int64_t cur_bt = -1;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        int cur_bt = -1;
         int nb = 0;
-        const int pieces_per_row = c.nchunk * kPiecesPerChunk;
-        const int total = kTileM * pieces_per_row;
-        const uint8_t *lat = static_cast<const uint8_t *>(p.latent);
-        UnitIter it(u_begin, c.NT);
-        for (int64_t u = u_begin; u < u_end; ++u, it.next()) {
-            const int64_t bt = it.bt;
-            const int tile = it.tile;
-            if (tile * kTileM >= unit_valid_len<kGather>(p, bt))
-                continue;
-            const int b = seq_of(bt, p.T);
-            if (bt != cur_bt) {
-                if (warp == 0) {
-                    bool ok = true;
-                    if (lane == 0) {
-                        if (nb > 0)
-                            ok = mbar_wait(&bars->b_empty, (nb - 1) & 1, abort_flag, p.status,
-                                           kWaitLimitNs);
-                        if (ok) {
-                            mbar_arrive_expect_tx(&bars->b_full,
-                                                  static_cast<uint32_t>(c.nchunk * c.b_chunk_bytes));
-                            const int row0 = static_cast<int>((bt * p.Gtot + p.g0) * p.H);
-                            for (int ch = 0; ch < c.nchunk; ++ch)
-                                tma_load_2d(smB + ch * c.b_chunk_bytes, &tmB, &bars->b_full,
-                                            ch * kChunkElems, row0);
-                        }
-                    }
-                    if (__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) == 0)
-                        break;
-                }
-                cur_bt = bt;
+        uint32_t b_base = b_base0;
+        Walk<kGather> w;
+        for (w.init(p, u_begin, u_end, c.NT); w.ok(); w.next(p, c.NT)) {
+            if (w.bt != cur_bt) {
+                if (nb > 0 && lane == 0)
+                    umma_commit(&bars->b_empty[(nb - 1) % c.nbuf]);
+                const int bb = nb % c.nbuf;
+                if (!warp_wait(&bars->b_full[bb], static_cast<uint32_t>(nb / c.nbuf) & 1u, abort_flag,
+                               p.status))
+                    break;
+                b_base = b_base0 + static_cast<uint32_t>(bb * c.b_buf_stride);
+                cur_bt = w.bt;
                 ++nb;
             }
-            if (!warp_wait(&empty[stage], phase ^ 1u, abort_flag, p.status))
+            if (!warp_wait(&bars->tmem_empty[acc], acc_phase ^ 1u, abort_flag, p.status))
                 break;
-            uint8_t *dstA = smA + stage * c.a_stage_bytes;
-            const int32_t *gidx = p.gather_idx + static_cast<int64_t>(b) * p.L_out;
-            for (int q = pid; q < total; q += 96) {
-                const int row = q / pieces_per_row;
-                const int j = q % pieces_per_row;
-                const int ch = j / kPiecesPerChunk;
-                const int qc = j % kPiecesPerChunk;
-                const int slot = tile * kTileM + row;
-                uint4 v = make_uint4(0u, 0u, 0u, 0u);
-                if (slot < p.n_gather) {
-                    const int idx = __ldg(gidx + slot);
-                    if (idx >= 0 && idx < p.L_lat) {
-                        const uint8_t *src = lat +
-                                             ((static_cast<int64_t>(b) * p.L_lat + idx) * p.r +
-                                              ch * kChunkElems) * kEsz + qc * kPiece;
-                        v = __ldg(reinterpret_cast<const uint4 *>(src));
-                    } else {
-                        atomicCAS(p.status, 0, -7 /* LI_ERR_DEVICE_BOUNDS */);
-                    }
-                }
-                uint32_t off = static_cast<uint32_t>(row * (kChunkElems * kEsz) + qc * kPiece);
-                off ^= ((off >> 7) & (kFP8 ? 3u : 7u)) << 4;
-                *reinterpret_cast<uint4 *>(dstA + ch * c.a_chunk_bytes + off) = v;
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&full[stage]);
-            if (++stage == c.stages) {
-                stage = 0;
-                phase ^= 1u;
-            }
-        }
-        if (warp == 0 && lane == 0 && nb > 0)
-            mbar_wait(&bars->b_full, (nb - 1) & 1, abort_flag, p.status, kWaitLimitNs);
-        __syncwarp();
-    } else if (warp == 1) {
-        // ---------------------------------------------------------- MMA issuer
-        if (lane == 0) {
-            const uint32_t idesc = umma_idesc(kFP8, kTileM, c.N);
-            const uint32_t a_base = smem_u32(smA);
-            const uint32_t b_base = smem_u32(smB);
-            int stage = 0;
-            uint32_t phase = 0;
-            int acc = 0;
-            uint32_t acc_phase = 0;
-            int64_t cur_bt = -1;
-            int nb = 0;
-            UnitIter it(u_begin, c.NT);
-            for (int64_t u = u_begin; u < u_end; ++u, it.next()) {
-                const int64_t bt = it.bt;
-                const int tile = it.tile;
-                if (tile * kTileM >= unit_valid_len<kGather>(p, bt))
-                    continue;
-                if (bt != cur_bt) {
-                    if (nb > 0)
-                        umma_commit(&bars->b_empty);
-                    if (!mbar_wait(&bars->b_full, nb & 1, abort_flag, p.status, kWaitLimitNs))
-                        break;
-                    cur_bt = bt;
-                    ++nb;
-                }
-                if (!mbar_wait(&bars->tmem_empty[acc], acc_phase ^ 1u, abort_flag, p.status,
-                               kWaitLimitNs))
-                    break;
-                if (!mbar_wait(&full[stage], phase, abort_flag, p.status, kWaitLimitNs))
-                    break;
-                tc_fence_after();
-                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * c.acc_stride);
+            if (!warp_wait(&full[stage], phase, abort_flag, p.status))
+                break;
+            tc_fence_after();
+            if (lane == 0) {
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kAccStride);
                 const uint32_t a_stage = a_base + static_cast<uint32_t>(stage * c.a_stage_bytes);
                 for (int ch = 0; ch < c.nchunk; ++ch) {
 #pragma unroll
@@ -371,146 +326,344 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 umma_commit(&empty[stage]);
                 umma_commit(&bars->tmem_full[acc]);
-                if (++stage == c.stages) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
-                acc ^= 1;
-                if (acc == 0)
-                    acc_phase ^= 1u;
             }
-            // all MMAs issued by this thread have completed before TMEM is freed
-            umma_commit(&bars->done);
-            mbar_wait(&bars->done, 0, abort_flag, p.status, kWaitLimitNs);
-        }
-        __syncwarp();
-    } else if (warp >= 4) {
-        // ------------------------------------------------------------ epilogue
-        constexpr int CH = kH < 32 ? kH : 32;          // TMEM columns per load
-        constexpr int CPL = kH / CH;                   // loads per layer
-        const int e = warp - 4;                        // 0..7
-        const int quarter = warp & 3;                  // TMEM lane quarter
-        const int lper = (Gs + 1) / 2;
-        const int l_begin = (e >> 2) * lper;
-        const int l_end = min(Gs, l_begin + lper);
-        const int nlay = l_end > l_begin ? l_end - l_begin : 0;
-        const int nchunks = nlay * CPL;
-        const int row = quarter * 32 + lane;
-        float *wq = misc->wq[e];
-        float *sq = misc->sq[e];
-        float *bq = misc->bq[e];
-        int acc = 0;
-        uint32_t acc_phase = 0;
-        int64_t cur_bt = -1;
-        UnitIter it(u_begin, c.NT);
-        for (int64_t u = u_begin; u < u_end; ++u, it.next()) {
-            const int64_t bt = it.bt;
-            const int tile = it.tile;
-            const int Lv = unit_valid_len<kGather>(p, bt);
-            if (tile * kTileM >= Lv)
-                continue;
-            const int b = seq_of(bt, p.T);
-            if (bt != cur_bt) {
-                __syncwarp();
-                const int64_t wrow = (bt * p.Gtot + p.g0 + l_begin) * p.H;
-                for (int j = lane; j < nlay * kH; j += 32) {
-                    const float wv = p.w[wrow + j];
-                    const float sv = p.q_abs_scale ? p.q_abs_scale[wrow + j] : 1.f;
-                    if (kBeta) {
-                        wq[j] = wv;
-                        sq[j] = sv;
-                        bq[j] = p.beta[wrow + j];
-                    } else {
-                        wq[j] = wv * sv;
-                    }
-                }
-                __syncwarp();
-                cur_bt = bt;
-            }
-            if (!warp_wait(&bars->tmem_full[acc], acc_phase, abort_flag, p.status))
-                break;
-            tc_fence_after();
-            const int pos = tile * kTileM + row;
-            const bool valid = pos < Lv;
-            float sc = 1.f;
-            if (p.lat_scale != nullptr) {
-                sc = 0.f;
-                if (valid) {
-                    int tok = pos;
-                    if (kGather)
-                        tok = p.gather_idx[static_cast<int64_t>(b) * p.L_out + pos];
-                    if (tok >= 0 && tok < p.L_lat)
-                        sc = p.lat_scale[static_cast<int64_t>(b) * p.L_lat + tok];
-                }
-            }
-            const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                                   static_cast<uint32_t>(acc * c.acc_stride + l_begin * kH);
-            float *out = p.scores + (bt * Gs + l_begin) * static_cast<int64_t>(p.L_out) + pos;
-
-            float2 s2a = make_float2(0.f, 0.f), s2b = make_float2(0.f, 0.f);
-            // reduce one chunk of CH head columns into the running layer sum
-            auto consume = [&](int i, const uint32_t (&v)[CH]) {
-                const int col = i * CH;
-                if (kBeta) {
-#pragma unroll
-                    for (int j = 0; j < CH; j += 2) {
-                        const float x0 = fmaf(__uint_as_float(v[j]) * sq[col + j], sc, bq[col + j]);
-                        const float x1 = fmaf(__uint_as_float(v[j + 1]) * sq[col + j + 1], sc, bq[col + j + 1]);
-                        s2a = __ffma2_rn(make_float2(wq[col + j], wq[col + j + 1]),
-                                         make_float2(fmaxf(x0, 0.f), fmaxf(x1, 0.f)), s2a);
-                    }
-                } else {
-                    const float4 *w4 = reinterpret_cast<const float4 *>(wq + col);
-#pragma unroll
-                    for (int j = 0; j < CH; j += 4) {
-                        const float4 ww = w4[j / 4];
-                        s2a = __ffma2_rn(make_float2(ww.x, ww.y),
-                                         make_float2(fmaxf(__uint_as_float(v[j]), 0.f),
-                                                     fmaxf(__uint_as_float(v[j + 1]), 0.f)), s2a);
-                        s2b = __ffma2_rn(make_float2(ww.z, ww.w),
-                                         make_float2(fmaxf(__uint_as_float(v[j + 2]), 0.f),
-                                                     fmaxf(__uint_as_float(v[j + 3]), 0.f)), s2b);
-                    }
-                }
-                if ((i + 1) % CPL == 0) {
-                    float uval = (s2a.x + s2a.y) + (s2b.x + s2b.y);
-                    if (!kBeta)
-                        uval *= sc;
-                    if (valid)
-                        out[static_cast<int64_t>(i / CPL) * p.L_out] = uval;
-                    s2a = make_float2(0.f, 0.f);
-                    s2b = make_float2(0.f, 0.f);
-                }
-            };
-            uint32_t va[CH], vb[CH];
-            if (nchunks > 0)
-                tmem_ld_chunk(tbase, va);
-            for (int i = 0; i < nchunks; i += 2) {
-                tmem_wait_chunk(va);
-                if (i + 1 < nchunks)
-                    tmem_ld_chunk(tbase + static_cast<uint32_t>((i + 1) * CH), vb);
-                consume(i, va);
-                if (i + 1 < nchunks) {
-                    tmem_wait_chunk(vb);
-                    if (i + 2 < nchunks)
-                        tmem_ld_chunk(tbase + static_cast<uint32_t>((i + 2) * CH), va);
-                    consume(i + 1, vb);
-                }
-            }
-            tc_fence_before();
             __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&bars->tmem_empty[acc]);
+            if (++stage == c.stages) {
+                stage = 0;
+                phase ^= 1u;
+            }
             acc ^= 1;
             if (acc == 0)
                 acc_phase ^= 1u;
         }
+        // all MMAs issued by lane 0 have completed before TMEM is freed
+        if (lane == 0)
+            umma_commit(&bars->done);
+        __syncwarp();
+        mbar_wait(&bars->done, 0, abort_flag, p.status, kWaitLimitNs);
+        __syncwarp();
+    } else if (!kGather && warp == R::kProdWarp0) {
+        // ------------------------------------------------------ TMA producer
+        // The warp walks the units together; lane 0 issues the copies.
+        if (lane == 0) {
+            tma_prefetch_desc(&tmA);
+            tma_prefetch_desc(&tmB);
+        }
+        const uint64_t pol = make_l2_policy(p.T == 1);   // decode: each tile is read once
+        int stage = 0;
+        uint32_t phase = 0;
+        int cur_bt = -1;
+        int nb = 0;
+        int issued = 0;
+        Walk<kGather> w;
+        for (w.init(p, u_begin, u_end, c.NT); w.ok(); w.next(p, c.NT)) {
+            if (w.bt != cur_bt) {
+                if (!load_query_operand(w.bt, nb))
+                    break;
+                cur_bt = w.bt;
+                ++nb;
+            }
+            if (!warp_wait(&empty[stage], phase ^ 1u, abort_flag, p.status))
+                break;
+            if (lane == 0) {
+                uint8_t *dstA = smA + stage * c.a_stage_bytes;
+                mbar_arrive_expect_tx(&full[stage], static_cast<uint32_t>(c.a_stage_bytes));
+                const int b = seq_of(w.bt, p.T);
+                for (int ch = 0; ch < c.nchunk; ++ch)
+                    tma_load_3d_hint(dstA + ch * c.a_chunk_bytes, &tmA, &full[stage],
+                                     ch * kChunkElems, w.tile * kTileM, b, pol);
+            }
+            __syncwarp();
+            ++issued;
+            if (++stage == c.stages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+        // Never leave the CTA with copies in flight: wait (bounded) for the
+        // last load issued into each stage and for the last query operands.
+        for (int s2 = 0; s2 < c.stages && s2 < issued; ++s2) {
+            const int last = s2 + (issued - 1 - s2) / c.stages * c.stages;   // last tile into s2
+            mbar_wait(&full[s2], static_cast<uint32_t>(last / c.stages) & 1u, abort_flag, p.status,
+                      kWaitLimitNs);
+        }
+        drain_query_operand(nb);
+        __syncwarp();
+    } else if (kGather && warp >= R::kProdWarp0 && warp < R::kEpiWarp0) {
+        // ------------------------------- gather producer (2 warps, 64 threads)
+        // Thread t copies tile rows t and t + 64 of every unit: the gathered
+        // latent rows, as 16-byte cp.async into the swizzled K-major layout TMA
+        // would write (zeros past the candidate count).  Up to c.gdepth tiles
+        // are in flight per thread; a tile's full barrier gets one arrival per
+        // warp once the warp's copies of it have landed.  Lane 0 of the first
+        // warp also loads the query operand by TMA.
+        constexpr int kRowsPerThread = kTileM / (32 * R::kProdWarps);
+        const int t0 = (warp - R::kProdWarp0) * 32 + lane;
+        const bool qloader = warp == R::kProdWarp0;
+        if (qloader && lane == 0)
+            tma_prefetch_desc(&tmB);
+        const uint8_t *lat = static_cast<const uint8_t *>(p.latent);
+        const int row_bytes = p.r * kEsz;
+        const int pieces = c.nchunk * kPiecesPerChunk;
+        const uint32_t a_base = smem_u32(smA);
+        int stage = 0;
+        uint32_t phase = 0;
+        int pend = 0;
+        int cur_bt = -1;
+        int nb = 0;
+        auto load_idx = [&](const Walk<kGather> &x, int row) -> int {
+            const int slot = x.tile * kTileM + row;
+            if (!x.ok() || slot >= p.n_gather)
+                return -1;
+            return __ldg(p.gather_idx + static_cast<int64_t>(seq_of(x.bt, p.T)) * p.L_out + slot);
+        };
+        auto signal_oldest = [&]() {
+            int s_old = stage - pend;
+            if (s_old < 0)
+                s_old += c.stages;
+            if (lane == 0)
+                mbar_arrive(&full[s_old]);
+            --pend;
+        };
+        Walk<kGather> w;
+        w.init(p, u_begin, u_end, c.NT);
+        int idx_next[kRowsPerThread];
+#pragma unroll
+        for (int i = 0; i < kRowsPerThread; ++i)
+            idx_next[i] = load_idx(w, t0 + 32 * R::kProdWarps * i);
+        while (w.ok()) {
+            Walk<kGather> wn = w;
+            wn.next(p, c.NT);
+            int idx[kRowsPerThread];
+#pragma unroll
+            for (int i = 0; i < kRowsPerThread; ++i) {
+                idx[i] = idx_next[i];
+                idx_next[i] = load_idx(wn, t0 + 32 * R::kProdWarps * i);   // one tile ahead
+            }
+            if (w.bt != cur_bt) {
+                if (qloader && !load_query_operand(w.bt, nb))
+                    break;
+                cur_bt = w.bt;
+                ++nb;
+            }
+            if (!warp_wait(&empty[stage], phase ^ 1u, abort_flag, p.status))
+                break;
+            const int b = seq_of(w.bt, p.T);
+            const uint32_t dst0 = a_base + static_cast<uint32_t>(stage * c.a_stage_bytes);
+#pragma unroll
+            for (int i = 0; i < kRowsPerThread; ++i) {
+                const int row = t0 + 32 * R::kProdWarps * i;
+                const int slot = w.tile * kTileM + row;
+                const bool in = slot < p.n_gather;
+                const bool valid = in && idx[i] >= 0 && idx[i] < p.L_lat;
+                if (in && !valid)
+                    atomicCAS(p.status, 0, -7 /* LI_ERR_DEVICE_BOUNDS */);
+                const uint8_t *src =
+                    lat + (static_cast<int64_t>(b) * p.L_lat + (valid ? idx[i] : 0)) * row_bytes;
+                const uint32_t nbytes = valid ? 16u : 0u;
+                for (int j = 0; j < pieces; ++j) {
+                    const int ch = j / kPiecesPerChunk;
+                    const int qc = j % kPiecesPerChunk;
+                    uint32_t off = static_cast<uint32_t>(row * kRowChunkBytes + qc * 16);
+                    off ^= ((off >> 7) & (kFP8 ? 3u : 7u)) << 4;
+                    cp_async_16(dst0 + static_cast<uint32_t>(ch * c.a_chunk_bytes) + off, src + j * 16,
+                                nbytes);
+                }
+            }
+            cp_async_commit();
+            ++pend;
+            if (++stage == c.stages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+            if (pend > c.gdepth) {
+                cp_async_wait_depth(c.gdepth);
+                fence_proxy_async_smem();
+                __syncwarp();
+                signal_oldest();
+            }
+            w = wn;
+        }
+        // every copy this thread issued lands before the CTA can exit
+        cp_async_wait_group<0>();
+        fence_proxy_async_smem();
+        __syncwarp();
+        while (pend > 0)
+            signal_oldest();
+        if (qloader)
+            drain_query_operand(nb);
+        __syncwarp();
+    } else if (warp >= R::kEpiWarp0) {
+        // ------------------------------------------------------------ epilogue
+        const int e = warp - R::kEpiWarp0;          // 0..15
+        const int quarter = warp & 3;               // TMEM lane quarter
+        const int c0 = (e >> 2) * c.cw;             // first accumulator column
+        if (c0 < c.N) {
+            const int ncols = min(c.cw, c.N - c0);
+            const int l0 = c0 / kH;                 // first layer (within the Gs scored)
+            const int nlay = (ncols + kH - 1) / kH;
+            const int row = quarter * 32 + lane;
+            float *wq = misc->wq + e * c.cw;
+            float *sq = misc->sq + e * c.cw;
+            float *bq = misc->bq + e * c.cw;
+            const uint32_t tq = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                static_cast<uint32_t>(c0);
+
+            // per-token scale: one tile ahead (scan), or index two tiles and
+            // scale one tile ahead (gather)
+            auto tok_of = [&](const Walk<kGather> &x) -> int {
+                const int pos = x.tile * kTileM + row;
+                if (!x.ok() || pos >= x.Lv)
+                    return -1;
+                if (kGather)
+                    return __ldg(p.gather_idx + static_cast<int64_t>(seq_of(x.bt, p.T)) * p.L_out + pos);
+                return pos;
+            };
+            auto scale_of = [&](const Walk<kGather> &x, int tok) -> float {
+                if (p.lat_scale == nullptr)
+                    return 1.f;
+                if (tok < 0 || tok >= p.L_lat)
+                    return 0.f;
+                return __ldg(p.lat_scale + static_cast<int64_t>(seq_of(x.bt, p.T)) * p.L_lat + tok);
+            };
+
+            Walk<kGather> w;
+            w.init(p, u_begin, u_end, c.NT);
+            float sc_cur = scale_of(w, tok_of(w));
+            float sc_next = 0.f;
+            int tok1 = 0;                           // gather: token of the next unit
+            if (kGather) {
+                Walk<kGather> t = w;
+                t.next(p, c.NT);
+                tok1 = tok_of(t);
+            }
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            int cur_bt = -1;
+            while (w.ok()) {
+                int tok2 = 0;
+                {
+                    // look ahead: the next unit's scale (its gathered index was
+                    // loaded a tile ago) and, when gathering, the index after it
+                    Walk<kGather> t = w;
+                    t.next(p, c.NT);
+                    sc_next = scale_of(t, kGather ? tok1 : tok_of(t));
+                    if (kGather) {
+                        t.next(p, c.NT);
+                        tok2 = tok_of(t);
+                    }
+                }
+                if (w.bt != cur_bt) {
+                    __syncwarp();
+                    const int64_t wrow = (w.bt * p.Gtot + p.g0) * p.H + c0;
+                    for (int j = lane; j < ncols; j += 32) {
+                        const float wv = p.w[wrow + j];
+                        const float sv = p.q_abs_scale ? p.q_abs_scale[wrow + j] : 1.f;
+                        if (kBeta) {
+                            wq[j] = wv;
+                            sq[j] = sv;
+                            bq[j] = p.beta[wrow + j];
+                        } else {
+                            wq[j] = wv * sv;
+                        }
+                    }
+                    __syncwarp();
+                    cur_bt = w.bt;
+                }
+                if (!warp_wait(&bars->tmem_full[acc], acc_phase, abort_flag, p.status))
+                    break;
+                tc_fence_after();
+                const int pos = w.tile * kTileM + row;
+                const bool valid = pos < w.Lv;
+                const float sc = sc_cur;
+                float *out = p.scores + (w.bt * Gs + l0) * static_cast<int64_t>(p.L_out) + pos;
+                const uint32_t tacc = tq + static_cast<uint32_t>(acc * kAccStride);
+
+                auto finish = [&](int lay, float u) {
+                    if (!kBeta)
+                        u *= sc;
+                    if (valid && lay < nlay)
+                        out[static_cast<int64_t>(lay) * p.L_out] = u;
+                };
+                float2 a0 = make_float2(0.f, 0.f), a1 = a0, a2 = a0, a3 = a0;
+                // 32 accumulator columns starting at column `col` (relative to
+                // c0) into the running sums (x, y)
+                auto chunk = [&](const uint32_t(&v)[32], int col, float2 &x, float2 &y) {
+                    if (kBeta) {
+#pragma unroll
+                        for (int j = 0; j < 32; j += 2) {
+                            const float x0 = fmaf(__uint_as_float(v[j]) * sq[col + j], sc, bq[col + j]);
+                            const float x1 = fmaf(__uint_as_float(v[j + 1]) * sq[col + j + 1], sc,
+                                                  bq[col + j + 1]);
+                            x = __ffma2_rn(make_float2(wq[col + j], wq[col + j + 1]),
+                                           make_float2(fmaxf(x0, 0.f), fmaxf(x1, 0.f)), x);
+                            if (kH == 16 && (j == 14 || j == 30)) {
+                                finish((col + j) / 16, x.x + x.y);
+                                x = make_float2(0.f, 0.f);
+                            }
+                        }
+                    } else {
+                        const float4 *w4 = reinterpret_cast<const float4 *>(wq + col);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const float4 ww = w4[j];
+                            x = __ffma2_rn(make_float2(ww.x, ww.y),
+                                           make_float2(fmaxf(__uint_as_float(v[4 * j]), 0.f),
+                                                       fmaxf(__uint_as_float(v[4 * j + 1]), 0.f)), x);
+                            y = __ffma2_rn(make_float2(ww.z, ww.w),
+                                           make_float2(fmaxf(__uint_as_float(v[4 * j + 2]), 0.f),
+                                                       fmaxf(__uint_as_float(v[4 * j + 3]), 0.f)), y);
+                            if (kH == 16 && (j == 3 || j == 7)) {
+                                finish((col + 4 * j) / 16, (x.x + x.y) + (y.x + y.y));
+                                x = make_float2(0.f, 0.f);
+                                y = x;
+                            }
+                        }
+                    }
+                    if (kH == 32) {
+                        finish(col / 32, (x.x + x.y) + (y.x + y.y));
+                        x = make_float2(0.f, 0.f);
+                        y = x;
+                    }
+                };
+                for (int cb = 0; cb < ncols; cb += 64) {
+                    uint32_t va[32], vb[32];
+                    tmem_ld32(tacc + static_cast<uint32_t>(cb), va);
+                    tmem_ld32(tacc + static_cast<uint32_t>(cb + 32), vb);
+                    tmem_ld_wait32(va);
+                    tmem_regs_ready(vb);
+                    if (cb + 64 >= ncols) {
+                        // the whole block is in registers: release the accumulator
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0)
+                            mbar_arrive(&bars->tmem_empty[acc]);
+                    }
+                    chunk(va, cb, a0, a1);
+                    chunk(vb, cb + 32, a2, a3);
+                    if (kH >= 64 && ((cb + 64) % kH) == 0) {
+                        finish((cb + 63) / kH, ((a0.x + a0.y) + (a1.x + a1.y)) +
+                                                   ((a2.x + a2.y) + (a3.x + a3.y)));
+                        a0 = make_float2(0.f, 0.f);
+                        a1 = a0;
+                        a2 = a0;
+                        a3 = a0;
+                    }
+                }
+                w.next(p, c.NT);
+                sc_cur = sc_next;
+                tok1 = tok2;
+                acc ^= 1;
+                if (acc == 0)
+                    acc_phase ^= 1u;
+            }
+        }
     }
 
     __syncthreads();
-    if (warp == 1) {
+    if (warp == R::kMmaWarp) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, static_cast<uint32_t>(c.tmem_cols));
+        tmem_dealloc(tmem_base, static_cast<uint32_t>(kTmemCols));
     }
 }
 
@@ -559,31 +712,38 @@ bool make_config(const ScoreParams &p, bool fp8, TcConfig &c, int &smem_bytes)
     c.a_chunk_bytes = kTileM * kChunkElems * esz;
     c.b_chunk_bytes = c.N * kChunkElems * esz;
     c.a_stage_bytes = c.nchunk * c.a_chunk_bytes;
-    const int b_bytes = c.nchunk * c.b_chunk_bytes;
-    const int b_bytes_al = (b_bytes + 1023) & ~1023;
-    int stages = (kSmemBudget - b_bytes_al - 4096) / c.a_stage_bytes;
+    c.b_bytes = c.nchunk * c.b_chunk_bytes;
+    c.b_buf_stride = (c.b_bytes + 1023) & ~1023;
+    const int bar_bytes = 2 * 8 * 8 + static_cast<int>(sizeof(Bars));
+    const int fixed = 1024 /* alignment slack */ + ((bar_bytes + 15) & ~15) +
+                      static_cast<int>(sizeof(Misc));
+    // Two query-operand buffers when that still leaves >= 3 latent stages.
+    int stages = (kSmemLimit - fixed - 2 * c.b_buf_stride) / c.a_stage_bytes;
+    c.nbuf = 2;
+    if (stages < 3) {
+        c.nbuf = 1;
+        stages = (kSmemLimit - fixed - c.b_buf_stride) / c.a_stage_bytes;
+    }
     if (stages > 8)
         stages = 8;
     if (stages < 2)
         return false;
     c.stages = stages;
-    c.off_a = b_bytes_al;
+    c.off_a = c.nbuf * c.b_buf_stride;
     c.off_bar = c.off_a + stages * c.a_stage_bytes;
-    const int bar_bytes = 2 * stages * 8 + static_cast<int>(sizeof(Bars));
-    c.off_misc = (c.off_bar + bar_bytes + 15) & ~15;
+    c.off_misc = (c.off_bar + 2 * stages * 8 + static_cast<int>(sizeof(Bars)) + 15) & ~15;
     smem_bytes = c.off_misc + static_cast<int>(sizeof(Misc)) + 1024;
     // one CTA per SM: a second CTA would only queue on the TMEM allocation
     if (smem_bytes < 116 * 1024)
         smem_bytes = 116 * 1024;
-    int cols = 32;
-    while (cols < 2 * c.N)
-        cols <<= 1;
-    c.tmem_cols = cols;
-    c.acc_stride = cols / 2;
+    c.cw = p.H >= 64 ? p.H : 64;
+    c.nepi = 4 * ((c.N + c.cw - 1) / c.cw);
+    c.gdepth = stages - 1 < 3 ? stages - 1 : 3;
     const int Lrow = p.gather_idx ? p.L_out : p.L_lat;
     c.NT = (Lrow + kTileM - 1) / kTileM;
     c.U = static_cast<int64_t>(p.B) * p.T * c.NT;
-    return smem_bytes <= 227 * 1024 && cols <= 512;
+    return smem_bytes <= kSmemLimit && c.nepi <= kEpiWarps && c.nepi * c.cw <= kConstCap &&
+           c.cw <= 128;
 }
 
 template <bool kFP8, bool kGather, bool kBeta, int kH>
@@ -598,17 +758,17 @@ cudaError_t launch_t(const CUtensorMap &tmA, const CUtensorMap &tmB, const Score
         dev = 0;
     if (set_bytes[dev].load(std::memory_order_relaxed) < smem_bytes) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             227 * 1024);
+                                             kSmemLimit);
         if (e != cudaSuccess)
             return e;
-        set_bytes[dev].store(227 * 1024, std::memory_order_relaxed);
+        set_bytes[dev].store(kSmemLimit, std::memory_order_relaxed);
     }
     int64_t grid = sm_count();
     if (grid > c.U)
         grid = c.U;
     if (grid <= 0)
         return cudaSuccess;
-    kern<<<static_cast<unsigned>(grid), kThreads, smem_bytes, s>>>(tmA, tmB, p, c);
+    kern<<<static_cast<unsigned>(grid), Roles<kGather>::kThreads, smem_bytes, s>>>(tmA, tmB, p, c);
     return cudaGetLastError();
 }
 
