@@ -45,6 +45,18 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar)
         : "memory");
 }
 
+// Arrive without release semantics: the arrival does not wait for this
+// thread's earlier global loads and stores to be performed.  For signals that
+// order only tensor-memory reads (made complete by tcgen05.wait::ld and
+// ordered by tcgen05.fence::before_thread_sync), not memory the waiter reads.
+__device__ __forceinline__ void mbar_arrive_relaxed(uint64_t *bar)
+{
+    asm volatile(
+        "{\n\t.reg .b64 st;\n\t"
+        "mbarrier.arrive.relaxed.cta.shared::cta.b64 st, [%0];\n\t}" ::"r"(smem_u32(bar))
+        : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
 {
     asm volatile(

@@ -19,15 +19,17 @@
 //
 // Roles (one persistent CTA per SM, static contiguous split of the
 // (query row, 128-token tile) work units; every role walks the same units):
-//   warp 0          TMEM allocation and the single-thread MMA issuer
+//   warp 0          TMEM allocation; MMA issuer of the CTA's even tiles
+//   warp after the producers: MMA issuer of the odd tiles (two issuers keep
+//                   one tile's MMAs queued while the other's execute)
 //   warp 1          scan mode: TMA producer of the latent tiles (smem ring) and
 //                   of the absorbed-query operand (double-buffered when it
 //                   fits, so the next query's operand loads under the current
 //                   query's tiles)
-//   warps 1-4       gather mode (HS followers rescoring the anchor's
-//                   candidates): one thread per tile row copies its gathered
-//                   latent row with 16-byte cp.async into the swizzled layout
-//                   TMA would write, several tiles in flight per thread
+//   warps 1-2       gather mode (HS followers rescoring the anchor's
+//                   candidates): each thread copies two tile rows of gathered
+//                   latent with 16-byte cp.async into the swizzled layout TMA
+//                   would write, several tiles in flight per thread
 //   16 warps        epilogue, four per TMEM lane quarter (warp % 4), each
 //                   owning 64 (or H when H > 64) accumulator columns, i.e. one
 //                   layer at H = 64: both 32-column TMEM loads in flight, the
@@ -65,11 +67,12 @@ constexpr int kSmemLimit = 227 * 1024;
 
 template <bool kGather>
 struct Roles {
-    static constexpr int kMmaWarp = 0;
+    static constexpr int kMmaWarp = 0;                        // even tiles (accumulator 0)
     static constexpr int kProdWarp0 = 1;
     static constexpr int kProdWarps = kGather ? 2 : 1;
-    static constexpr int kEpiWarp0 = 1 + kProdWarps;
-    static constexpr int kThreads = 32 * (1 + kProdWarps + kEpiWarps);
+    static constexpr int kMmaWarp1 = kProdWarp0 + kProdWarps;  // odd tiles (accumulator 1)
+    static constexpr int kEpiWarp0 = kMmaWarp1 + 1;
+    static constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
 };
 
 struct TcConfig {
@@ -234,11 +237,11 @@ __global__ void __launch_bounds__(Roles<kGather>::kThreads, 1)
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&bars->b_full[a], 1u);
-            mbar_init(&bars->b_empty[a], 1u);
+            mbar_init(&bars->b_empty[a], 2u);      // one commit from each MMA warp
             mbar_init(&bars->tmem_full[a], 1u);
             mbar_init(&bars->tmem_empty[a], static_cast<uint32_t>(c.nepi));
         }
-        mbar_init(&bars->done, 1u);
+        mbar_init(&bars->done, 2u);
         misc->abort = 0;
         mbar_fence_init();
     }
@@ -276,21 +279,30 @@ __global__ void __launch_bounds__(Roles<kGather>::kThreads, 1)
                       p.status, kWaitLimitNs);
     };
 
-    if (warp == R::kMmaWarp) {
-        // ---------------------------------------------------------- MMA issuer
-        // The warp walks the units together; lane 0 issues the MMAs and commits.
+    if (warp == R::kMmaWarp || warp == R::kMmaWarp1) {
+        // --------------------------------------------------------- MMA issuers
+        // Two warps (on different SM sub-partitions) issue the MMAs: the first
+        // the CTA's even tiles into accumulator 0, the second its odd tiles
+        // into accumulator 1.  A tcgen05.mma issue stalls its warp until the
+        // tensor pipe has room, which with one issuer meant that the next
+        // tile's MMAs could not even be prepared while the current ones ran;
+        // with two, one warp's MMAs are queued while the other's execute.
+        // Both warps walk every unit (stage ring, query operand buffers), and
+        // lane 0 issues the MMAs and commits.
+        const int par = warp == R::kMmaWarp ? 0 : 1;
         const uint32_t idesc = umma_idesc(kFP8, kTileM, c.N);
         const uint32_t a_base = smem_u32(smA);
         const uint32_t b_base0 = smem_u32(smB);
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(par * kAccStride);
         int stage = 0;
         uint32_t phase = 0;
-        int acc = 0;
         uint32_t acc_phase = 0;
         int cur_bt = -1;
         int nb = 0;
+        int ord = 0;                                   // tile ordinal within the CTA
         uint32_t b_base = b_base0;
         Walk<kGather> w;
-        for (w.init(p, u_begin, u_end, c.NT); w.ok(); w.next(p, c.NT)) {
+        for (w.init(p, u_begin, u_end, c.NT); w.ok(); w.next(p, c.NT), ++ord) {
             if (w.bt != cur_bt) {
                 if (nb > 0 && lane == 0)
                     umma_commit(&bars->b_empty[(nb - 1) % c.nbuf]);
@@ -302,39 +314,38 @@ __global__ void __launch_bounds__(Roles<kGather>::kThreads, 1)
                 cur_bt = w.bt;
                 ++nb;
             }
-            if (!warp_wait(&bars->tmem_empty[acc], acc_phase ^ 1u, abort_flag, p.status))
-                break;
-            if (!warp_wait(&full[stage], phase, abort_flag, p.status))
-                break;
-            tc_fence_after();
-            if (lane == 0) {
-                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kAccStride);
-                const uint32_t a_stage = a_base + static_cast<uint32_t>(stage * c.a_stage_bytes);
-                for (int ch = 0; ch < c.nchunk; ++ch) {
+            if ((ord & 1) == par) {
+                if (!warp_wait(&bars->tmem_empty[par], acc_phase ^ 1u, abort_flag, p.status))
+                    break;
+                if (!warp_wait(&full[stage], phase, abort_flag, p.status))
+                    break;
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t a_stage = a_base + static_cast<uint32_t>(stage * c.a_stage_bytes);
+                    for (int ch = 0; ch < c.nchunk; ++ch) {
 #pragma unroll
-                    for (int ks = 0; ks < kStepsPerChunk; ++ks) {
-                        const uint64_t ad = umma_sdesc(
-                            a_stage + static_cast<uint32_t>(ch * c.a_chunk_bytes + ks * 32), kSbo, kSwz);
-                        const uint64_t bd = umma_sdesc(
-                            b_base + static_cast<uint32_t>(ch * c.b_chunk_bytes + ks * 32), kSbo, kSwz);
-                        const uint32_t accum = (ch | ks) != 0 ? 1u : 0u;
-                        if (kFP8)
-                            umma_fp8(d_tmem, ad, bd, idesc, accum);
-                        else
-                            umma_bf16(d_tmem, ad, bd, idesc, accum);
+                        for (int ks = 0; ks < kStepsPerChunk; ++ks) {
+                            const uint64_t ad = umma_sdesc(
+                                a_stage + static_cast<uint32_t>(ch * c.a_chunk_bytes + ks * 32), kSbo, kSwz);
+                            const uint64_t bd = umma_sdesc(
+                                b_base + static_cast<uint32_t>(ch * c.b_chunk_bytes + ks * 32), kSbo, kSwz);
+                            const uint32_t accum = (ch | ks) != 0 ? 1u : 0u;
+                            if (kFP8)
+                                umma_fp8(d_tmem, ad, bd, idesc, accum);
+                            else
+                                umma_bf16(d_tmem, ad, bd, idesc, accum);
+                        }
                     }
+                    umma_commit(&empty[stage]);
+                    umma_commit(&bars->tmem_full[par]);
                 }
-                umma_commit(&empty[stage]);
-                umma_commit(&bars->tmem_full[acc]);
+                __syncwarp();
+                acc_phase ^= 1u;
             }
-            __syncwarp();
             if (++stage == c.stages) {
                 stage = 0;
                 phase ^= 1u;
             }
-            acc ^= 1;
-            if (acc == 0)
-                acc_phase ^= 1u;
         }
         // all MMAs issued by lane 0 have completed before TMEM is freed
         if (lane == 0)
@@ -389,7 +400,7 @@ __global__ void __launch_bounds__(Roles<kGather>::kThreads, 1)
         }
         drain_query_operand(nb);
         __syncwarp();
-    } else if (kGather && warp >= R::kProdWarp0 && warp < R::kEpiWarp0) {
+    } else if (kGather && warp >= R::kProdWarp0 && warp < R::kProdWarp0 + R::kProdWarps) {
         // ------------------------------- gather producer (2 warps, 64 threads)
         // Thread t copies tile rows t and t + 64 of every unit: the gathered
         // latent rows, as 16-byte cp.async into the swizzled K-major layout TMA
@@ -633,11 +644,15 @@ __global__ void __launch_bounds__(Roles<kGather>::kThreads, 1)
                     tmem_ld_wait32(va);
                     tmem_regs_ready(vb);
                     if (cb + 64 >= ncols) {
-                        // the whole block is in registers: release the accumulator
+                        // The whole block is in registers: release the accumulator.
+                        // A relaxed arrival: a release would first wait for this
+                        // warp's outstanding global loads and stores (the next
+                        // tile's scale prefetch, the last tile's scores), which
+                        // holds the accumulator, and so the MMAs, ~1 us longer.
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0)
-                            mbar_arrive(&bars->tmem_empty[acc]);
+                            mbar_arrive_relaxed(&bars->tmem_empty[acc]);
                     }
                     chunk(va, cb, a0, a1);
                     chunk(vb, cb + 32, a2, a3);
