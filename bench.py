@@ -132,55 +132,57 @@ class L2Flush:
 # --------------------------------------------------------------------- clocks
 
 class ClockSampler:
+    """SM clock and clock-event (throttle) reasons of one GPU, read through NVML
+    (the library nvidia-smi itself uses), only ever reading settings.
+
+    Every NVML query briefly stalls the GPU's work (measured here: 0.3-3 ms per
+    query, which would inflate a ~30 ms timed region by several percent), so
+    the timed loop takes as few samples as the timing rules allow: one per
+    ~1000 steps and at least one, each taken while the GPU is still executing
+    the steps the host has already enqueued."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
     def __init__(self, index: int):
-        self.index = index
-        self.proc = None
-        self.path = None
-
-    def __enter__(self):
-        import tempfile
-        fd, self.path = tempfile.mkstemp(suffix=".csv")
-        os.close(fd)
-        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        import ctypes
+        self.samples = []
+        self.max_mhz = None
+        self.h = None
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={q}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
-        except (OSError, FileNotFoundError):
-            self.proc = None
-        time.sleep(0.3)
-        return self
+            self.nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nv.nvmlInit_v2() != 0:
+                return
+            h = ctypes.c_void_p()
+            if self.nv.nvmlDeviceGetHandleByIndex_v2(index, ctypes.byref(h)) != 0:
+                return
+            self.h = h
+            mx = ctypes.c_uint()
+            if self.nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:   # 1 = SM clock
+                self.max_mhz = float(mx.value)
+        except OSError:
+            self.h = None
 
-    def __exit__(self, *a):
-        if self.proc is not None:
-            self.proc.terminate()
-            try:
-                self.proc.wait(timeout=5)
-            except subprocess.TimeoutExpired:
-                self.proc.kill()
+    def sample(self):
+        if self.h is None:
+            return
+        import ctypes
+        clk, rs, pw = ctypes.c_uint(), ctypes.c_ulonglong(), ctypes.c_uint()
+        ok = self.nv.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(clk)) == 0
+        self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h, ctypes.byref(rs))
+        self.nv.nvmlDeviceGetPowerUsage(self.h, ctypes.byref(pw))
+        if ok:
+            self.samples.append((float(clk.value), int(rs.value), pw.value / 1000.0))
 
     def summary(self):
-        if self.proc is None or not self.path:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        rows = []
-        with open(self.path) as f:
-            for line in f:
-                parts = [x.strip() for x in line.split(",")]
-                if len(parts) >= 9:
-                    rows.append(parts)
-        os.unlink(self.path)
-        if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
-                "samples": len(rows), "power_w_max": max(float(r[3]) for r in rows
-                                                        if r[3].replace(".", "").isdigit()) if rows else None}
+        if self.h is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvml unavailable"]}
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["no samples"]}
+        reasons = sorted({name for _, r, _ in self.samples for bit, name in self.REASONS.items() if r & bit})
+        return {"sm_mhz": statistics.median(c for c, _, _ in self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(self.samples),
+                "power_w_max": max(w for _, _, w in self.samples), "source": "NVML, during the timed steps"}
 
 
 # ------------------------------------------------------------------ reference
@@ -309,13 +311,17 @@ def run_ours(a, w):
     barrier = (lambda: torch.distributed.barrier()) if ws > 1 else (lambda: None)
     barrier()
     torch.cuda.synchronize(dev)
-    with ClockSampler(local) as clk:
-        t_wall = time.perf_counter()
-        for i in range(K):
-            flush()
-            step(evs[i])
-        torch.cuda.synchronize(dev)
-        t_wall = time.perf_counter() - t_wall
+    clk = ClockSampler(local)
+    nsamp = max(1, min(8, K // 1000))
+    sample_at = {int((j + 0.5) * K / nsamp) for j in range(nsamp)}
+    t_wall = time.perf_counter()
+    for i in range(K):
+        flush()
+        step(evs[i])
+        if i in sample_at:
+            clk.sample()          # the GPU is still running the steps enqueued so far
+    torch.cuda.synchronize(dev)
+    t_wall = time.perf_counter() - t_wall
     barrier()
     st = li.li_device_status(stream)
     if st != 0:

@@ -257,6 +257,8 @@ __global__ void __launch_bounds__(kThreads) absorb_kernel(AbsorbParams p)
 
 cudaError_t launch_absorb(const AbsorbParams &p, cudaStream_t s)
 {
+    if (absorb_tc_supported(p))
+        return launch_absorb_tc(p, s);
     const int64_t nrows = static_cast<int64_t>(p.N) * p.H;
     const int64_t gx = (nrows + kRows - 1) / kRows;
     if (gx > 0x7FFFFFFF || p.G > 65535 || p.r > kMaxR)

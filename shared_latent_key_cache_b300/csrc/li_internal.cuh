@@ -5,11 +5,21 @@
 #include <cstddef>
 #include <cstdint>
 
+#include <cuda.h>           // CUtensorMap and the tensor-map encoder's types
 #include <cuda_runtime.h>
 
 #include "../../include/li.h"
 
 namespace li {
+
+// cuTensorMapEncodeTiled from the driver (looked up once), or nullptr.
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_fn();
+// Multiprocessors of the current device (cached per device).
+int sm_count();
 
 // Upper bound for any single mbarrier wait inside a kernel (ns).
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
@@ -24,6 +34,10 @@ struct AbsorbParams {
     int N, G, H, d, r;
 };
 cudaError_t launch_absorb(const AbsorbParams &p, cudaStream_t s);
+// Tensor-core absorption (bf16 q and D, 64 | d <= 256, 32 | r <= 256,
+// H in {16, 32, 64, 128}); launch_absorb uses it when it applies.
+bool absorb_tc_supported(const AbsorbParams &p);
+cudaError_t launch_absorb_tc(const AbsorbParams &p, cudaStream_t s);
 
 // ------------------------------------------------------------- scoring
 // One scoring launch evaluates eq. (8) for a contiguous range of Gs layers

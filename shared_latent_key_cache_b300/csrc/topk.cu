@@ -10,7 +10,9 @@
 // sort by (score desc, position asc): among keys equal to the k-th largest
 // the lowest positions are taken.
 //
-// One 1024-thread CTA per row, no global scratch memory:
+// Rows of at most 32,768 scores take the register-resident path below (one
+// read of the row, three histogram levels over the keys held in registers).
+// Longer rows: one 1024-thread CTA per row, no global scratch memory:
 //  1. Sampled thresholds (rows of >= 8192 valid scores selecting at most about
 //     a quarter of them): 4096 stratified samples are histogrammed (12 + 12
 //     key bits) to find two keys whose sample ranks sit five standard
@@ -570,6 +572,302 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p)
     }
 }
 
+
+// ------------------------------------------------------------------------
+// Register-resident path for rows of at most 32 * 1024 scores (the common
+// decode case): each thread keeps its 32 keys in registers and the row is
+// read from memory once.  The k-th largest key is found digit by digit with
+// shared-memory histograms over the keys' offsets from the row minimum
+// (11 + 11 + at most 10 bits; the first digit is chosen from the row's actual
+// key range, so its 2048 bins resolve the distribution where it is), then
+// every key above it is emitted and the ties at it are taken lowest position
+// first (ranked by ordered block scans only when there are more of them than
+// are needed).
+
+constexpr int kRegPer = 32;
+constexpr int kRegRow = kRegPer * kThreads;
+constexpr int kRBins = 2048;
+
+struct RegSmem {
+    uint32_t hist[kRBins];
+    uint32_t wa[kWarps];
+    uint32_t wb[kWarps];
+    uint32_t kmin, kmax;
+    int sel_bin;
+    uint32_t sel_gt;
+    int slot;
+};
+
+// Largest bin b (2 per thread) with  sum_{d >= b} hist[d] >= need; sets b and
+// the count strictly above it.  All threads must call.
+__device__ void reg_select_bin(RegSmem &sm, uint32_t need, int &bin, uint32_t &gt)
+{
+    const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+    const uint32_t h0 = sm.hist[2 * t], h1 = sm.hist[2 * t + 1];
+    const uint32_t local = h0 + h1;
+    uint32_t x = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t y = __shfl_down_sync(0xffffffffu, x, off);
+        if (lane + off < 32)
+            x += y;
+    }
+    if (lane == 0)
+        sm.wa[w] = x;
+    __syncthreads();
+    uint32_t s = x - local;
+    for (int w2 = w + 1; w2 < kWarps; ++w2)
+        s += sm.wa[w2];
+    if (s < need && s + h1 >= need) {
+        sm.sel_bin = 2 * t + 1;
+        sm.sel_gt = s;
+    }
+    s += h1;
+    if (s < need && s + h0 >= need) {
+        sm.sel_bin = 2 * t;
+        sm.sel_gt = s;
+    }
+    __syncthreads();
+    bin = sm.sel_bin;
+    gt = sm.sel_gt;
+    __syncthreads();
+}
+
+// Exclusive prefix sum of v over the block (thread order); *total = block sum.
+__device__ __forceinline__ uint32_t reg_excl_scan(RegSmem &sm, uint32_t v, uint32_t *total)
+{
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    uint32_t x = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, x, off);
+        if (lane >= off)
+            x += y;
+    }
+    if (lane == 31)
+        sm.wb[w] = x;
+    __syncthreads();
+    uint32_t base = 0, tot = 0;
+    for (int w2 = 0; w2 < kWarps; ++w2) {
+        const uint32_t c = sm.wb[w2];
+        base += w2 < w ? c : 0u;
+        tot += c;
+    }
+    *total = tot;
+    __syncthreads();
+    return base + x - v;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) topk_reg_kernel(const TopkParams p)
+{
+    __shared__ RegSmem sm;
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+
+    for (int64_t row = blockIdx.x; row < p.rows; row += gridDim.x) {
+        const float *src = p.scores + row * p.in_stride;
+        int V = p.L_row;
+        if (p.valid_len != nullptr) {
+            V = p.valid_len[row];
+            V = V < 0 ? 0 : (V > p.L_row ? p.L_row : V);
+        }
+        const int64_t grp = row / p.rows_per_group;
+        const int64_t orow = grp * p.group_stride + row % p.rows_per_group + p.row_offset;
+        int32_t *oidx = p.idx + orow * p.k;
+        float *oval = p.vals ? p.vals + orow * p.k : nullptr;
+        const int32_t *map = p.map ? p.map + grp * p.map_stride : nullptr;
+        const int nsel = p.k < V ? p.k : V;
+
+        for (int j = nsel + tid; j < p.k; j += kThreads) {      // padding
+            oidx[j] = -1;
+            if (oval)
+                oval[j] = -__int_as_float(0x7f800000);
+        }
+        if (nsel == V) {
+            for (int j = tid; j < V; j += kThreads) {
+                oidx[j] = map ? map[j] : j;
+                if (oval)
+                    oval[j] = src[j];
+            }
+            __syncthreads();
+            continue;
+        }
+
+        // ---- load: element e of this thread is at position 4 (tid + 1024 (e / 4)) + e % 4
+        uint32_t key[kRegPer];
+        const bool al16 = (reinterpret_cast<uintptr_t>(src) & 15u) == 0;
+#pragma unroll
+        for (int i = 0; i < kRegPer / 4; ++i) {
+            const int pos = 4 * (tid + kThreads * i);
+            if (al16 && pos + 3 < V) {
+                const float4 v = __ldg(reinterpret_cast<const float4 *>(src + pos));
+                key[4 * i] = float_key(v.x);
+                key[4 * i + 1] = float_key(v.y);
+                key[4 * i + 2] = float_key(v.z);
+                key[4 * i + 3] = float_key(v.w);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    key[4 * i + j] = pos + j < V ? float_key(__ldg(src + pos + j)) : 0u;
+            }
+        }
+        auto valid = [&](int e) { return 4 * (tid + kThreads * (e >> 2)) + (e & 3) < V; };
+
+        // ---- key range of the row
+        uint32_t lo = 0xFFFFFFFFu, hi = 0u;
+#pragma unroll
+        for (int e = 0; e < kRegPer; ++e)
+            if (valid(e)) {
+                lo = min(lo, key[e]);
+                hi = max(hi, key[e]);
+            }
+        lo = __reduce_min_sync(0xffffffffu, lo);
+        hi = __reduce_max_sync(0xffffffffu, hi);
+        if (lane == 0) {
+            sm.wa[w] = lo;
+            sm.wb[w] = hi;
+        }
+        __syncthreads();
+        if (tid == 0) {
+            uint32_t a = 0xFFFFFFFFu, b = 0u;
+            for (int w2 = 0; w2 < kWarps; ++w2) {
+                a = min(a, sm.wa[w2]);
+                b = max(b, sm.wb[w2]);
+            }
+            sm.kmin = a;
+            sm.kmax = b;
+            sm.slot = 0;
+        }
+        __syncthreads();
+        const uint32_t kmin = sm.kmin;
+        const uint32_t range = sm.kmax - kmin;
+        const int nbits = range ? 32 - __clz(range) : 0;
+        const int shift1 = nbits > 11 ? nbits - 11 : 0;
+        const int shift2 = shift1 > 11 ? shift1 - 11 : 0;
+
+        // ---- digits of the k-th largest offset (key - kmin)
+        uint32_t need = static_cast<uint32_t>(nsel);
+        uint32_t T = 0;          // offset of the threshold key
+        uint32_t cnt_eq = 0;     // keys equal to it
+        {
+            // level 1: bits [shift1, nbits)
+            for (int i = tid; i < kRBins; i += kThreads)
+                sm.hist[i] = 0u;
+            __syncthreads();
+#pragma unroll
+            for (int e = 0; e < kRegPer; ++e)
+                if (valid(e))
+                    atomicAdd(&sm.hist[(key[e] - kmin) >> shift1], 1u);
+            __syncthreads();
+            int b;
+            uint32_t gt;
+            reg_select_bin(sm, need, b, gt);
+            cnt_eq = sm.hist[b];
+            need -= gt;
+            T = static_cast<uint32_t>(b) << shift1;
+        }
+        if (shift1 > 0) {
+            // level 2: bits [shift2, shift1) of keys in the level-1 bin
+            const uint32_t m2 = (1u << (shift1 - shift2)) - 1u;
+            for (int i = tid; i < kRBins; i += kThreads)
+                sm.hist[i] = 0u;
+            __syncthreads();
+#pragma unroll
+            for (int e = 0; e < kRegPer; ++e) {
+                const uint32_t o = key[e] - kmin;
+                if (valid(e) && (o >> shift1) == (T >> shift1))
+                    atomicAdd(&sm.hist[(o >> shift2) & m2], 1u);
+            }
+            __syncthreads();
+            int b;
+            uint32_t gt;
+            reg_select_bin(sm, need, b, gt);
+            cnt_eq = sm.hist[b];
+            need -= gt;
+            T |= static_cast<uint32_t>(b) << shift2;
+        }
+        if (shift2 > 0) {
+            // level 3: bits [0, shift2) of keys matching the first two digits
+            const uint32_t m3 = (1u << shift2) - 1u;
+            for (int i = tid; i < kRBins; i += kThreads)
+                sm.hist[i] = 0u;
+            __syncthreads();
+#pragma unroll
+            for (int e = 0; e < kRegPer; ++e) {
+                const uint32_t o = key[e] - kmin;
+                if (valid(e) && (o >> shift2) == (T >> shift2))
+                    atomicAdd(&sm.hist[o & m3], 1u);
+            }
+            __syncthreads();
+            int b;
+            uint32_t gt;
+            reg_select_bin(sm, need, b, gt);
+            cnt_eq = sm.hist[b];
+            need -= gt;
+            T |= static_cast<uint32_t>(b);
+        }
+        const uint32_t K = kmin + T;     // the k-th largest key; `need` of its cnt_eq copies are taken
+
+        // ---- emit every key above K, positions in any order
+        uint32_t mine = 0;
+#pragma unroll
+        for (int e = 0; e < kRegPer; ++e)
+            mine += (valid(e) && key[e] > K) ? 1u : 0u;
+        uint32_t sure = 0;
+        uint32_t slot = reg_excl_scan(sm, mine, &sure);
+#pragma unroll
+        for (int e = 0; e < kRegPer; ++e) {
+            if (valid(e) && key[e] > K) {
+                const int pos = 4 * (tid + kThreads * (e >> 2)) + (e & 3);
+                oidx[slot] = map ? map[pos] : pos;
+                if (oval)
+                    oval[slot] = key_float(key[e]);
+                ++slot;
+            }
+        }
+        // ---- ties at K: all of them, or the `need` lowest positions
+        if (cnt_eq == need) {
+#pragma unroll
+            for (int e = 0; e < kRegPer; ++e) {
+                if (valid(e) && key[e] == K) {
+                    const int pos = 4 * (tid + kThreads * (e >> 2)) + (e & 3);
+                    const int s2 = static_cast<int>(sure) + atomicAdd(&sm.slot, 1);
+                    oidx[s2] = map ? map[pos] : pos;
+                    if (oval)
+                        oval[s2] = key_float(K);
+                }
+            }
+        } else {
+            uint32_t run = 0;
+#pragma unroll
+            for (int i = 0; i < kRegPer / 4; ++i) {
+                uint32_t c = 0;
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    c += (valid(4 * i + j) && key[4 * i + j] == K) ? 1u : 0u;
+                uint32_t tot = 0;
+                uint32_t r = run + reg_excl_scan(sm, c, &tot);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int e = 4 * i + j;
+                    if (valid(e) && key[e] == K) {
+                        if (r < need) {
+                            const int pos = 4 * (tid + kThreads * i) + j;
+                            oidx[sure + r] = map ? map[pos] : pos;
+                            if (oval)
+                                oval[sure + r] = key_float(K);
+                        }
+                        ++r;
+                    }
+                }
+                run += tot;
+                if (run >= need)
+                    break;          // uniform: every thread sees the same totals
+            }
+        }
+        __syncthreads();
+    }
+}
+
 } // namespace
 
 cudaError_t launch_topk(const TopkParams &p, cudaStream_t s)
@@ -590,7 +888,10 @@ cudaError_t launch_topk(const TopkParams &p, cudaStream_t s)
         attr_set[dev].store(1, std::memory_order_relaxed);
     }
     const int64_t grid = p.rows < 0x7FFFFFFF ? p.rows : 0x7FFFFFFF;
-    topk_kernel<<<static_cast<unsigned>(grid), kThreads, smem, s>>>(p);
+    if (p.L_row <= kRegRow)
+        topk_reg_kernel<<<static_cast<unsigned>(grid), kThreads, 0, s>>>(p);
+    else
+        topk_kernel<<<static_cast<unsigned>(grid), kThreads, smem, s>>>(p);
     return cudaGetLastError();
 }
 
