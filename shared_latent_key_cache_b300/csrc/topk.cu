@@ -588,15 +588,40 @@ constexpr int kRegPer = 32;
 constexpr int kRegRow = kRegPer * kThreads;
 constexpr int kRBins = 2048;
 
+constexpr int kRCap = 4096;       // candidate list (keys in the threshold bin)
+
 struct RegSmem {
     uint32_t hist[kRBins];
+    uint32_t ckey[kRCap];
+    int32_t cpos[kRCap];
     uint32_t wa[kWarps];
     uint32_t wb[kWarps];
     uint32_t kmin, kmax;
     int sel_bin;
     uint32_t sel_gt;
     int slot;
+    uint32_t out_cnt, cand_cnt;
 };
+
+// Warp-aggregated reservation of `n` consecutive slots per lane on a shared
+// counter; returns this lane's first slot.
+__device__ __forceinline__ uint32_t warp_reserve(uint32_t *counter, uint32_t n)
+{
+    const int lane = threadIdx.x & 31;
+    uint32_t x = n;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, x, off);
+        if (lane >= off)
+            x += y;
+    }
+    const uint32_t tot = __shfl_sync(0xffffffffu, x, 31);
+    uint32_t base = 0;
+    if (lane == 31 && tot > 0)
+        base = atomicAdd(counter, tot);
+    base = __shfl_sync(0xffffffffu, base, 31);
+    return base + x - n;
+}
 
 // Largest bin b (2 per thread) with  sum_{d >= b} hist[d] >= need; sets b and
 // the count strictly above it.  All threads must call.
@@ -710,7 +735,8 @@ __global__ void __launch_bounds__(kThreads, 1) topk_reg_kernel(const TopkParams 
                     key[4 * i + j] = pos + j < V ? float_key(__ldg(src + pos + j)) : 0u;
             }
         }
-        auto valid = [&](int e) { return 4 * (tid + kThreads * (e >> 2)) + (e & 3) < V; };
+        const bool full = V == kRegRow;
+        auto valid = [&](int e) { return full || 4 * (tid + kThreads * (e >> 2)) + (e & 3) < V; };
 
         // ---- key range of the row
         uint32_t lo = 0xFFFFFFFFu, hi = 0u;
@@ -736,6 +762,8 @@ __global__ void __launch_bounds__(kThreads, 1) topk_reg_kernel(const TopkParams 
             sm.kmin = a;
             sm.kmax = b;
             sm.slot = 0;
+            sm.out_cnt = 0;
+            sm.cand_cnt = 0;
         }
         __syncthreads();
         const uint32_t kmin = sm.kmin;
@@ -764,6 +792,121 @@ __global__ void __launch_bounds__(kThreads, 1) topk_reg_kernel(const TopkParams 
             cnt_eq = sm.hist[b];
             need -= gt;
             T = static_cast<uint32_t>(b) << shift1;
+        }
+        if (cnt_eq <= static_cast<uint32_t>(kRCap)) {
+            // ---- usual case: keys above the level-1 bin are selected now, the
+            // bin's keys move to a shared-memory list and the remaining digits
+            // and the ties are resolved on that list only
+            const uint32_t b1 = T >> shift1;
+            const uint32_t gt1 = static_cast<uint32_t>(nsel) - need;
+            uint32_t n_sure = 0, n_cand = 0;
+#pragma unroll
+            for (int e = 0; e < kRegPer; ++e) {
+                if (valid(e)) {
+                    const uint32_t bn = (key[e] - kmin) >> shift1;
+                    n_sure += bn > b1 ? 1u : 0u;
+                    n_cand += bn == b1 ? 1u : 0u;
+                }
+            }
+            uint32_t so = warp_reserve(&sm.out_cnt, n_sure);
+            uint32_t co = warp_reserve(&sm.cand_cnt, n_cand);
+#pragma unroll
+            for (int e = 0; e < kRegPer; ++e) {
+                if (valid(e)) {
+                    const uint32_t bn = (key[e] - kmin) >> shift1;
+                    const int pos = 4 * (tid + kThreads * (e >> 2)) + (e & 3);
+                    if (bn > b1) {
+                        oidx[so] = map ? map[pos] : pos;
+                        if (oval)
+                            oval[so] = key_float(key[e]);
+                        ++so;
+                    } else if (bn == b1) {
+                        sm.ckey[co] = key[e];
+                        sm.cpos[co] = pos;
+                        ++co;
+                    }
+                }
+            }
+            __syncthreads();
+            const int n = static_cast<int>(cnt_eq);
+            for (int level = 0; level < 2; ++level) {
+                const int hs = level == 0 ? shift1 : shift2;
+                const int ls = level == 0 ? shift2 : 0;
+                if (hs == 0)
+                    break;
+                const uint32_t msk = (1u << (hs - ls)) - 1u;
+                for (int i = tid; i < kRBins; i += kThreads)
+                    sm.hist[i] = 0u;
+                __syncthreads();
+                for (int i = tid; i < n; i += kThreads) {
+                    const uint32_t o = sm.ckey[i] - kmin;
+                    if ((o >> hs) == (T >> hs))
+                        atomicAdd(&sm.hist[(o >> ls) & msk], 1u);
+                }
+                __syncthreads();
+                int b;
+                uint32_t gt;
+                reg_select_bin(sm, need, b, gt);
+                cnt_eq = sm.hist[b];
+                need -= gt;
+                T |= static_cast<uint32_t>(b) << ls;
+            }
+            const uint32_t K = kmin + T;
+            // list keys above K
+            if (tid == 0)
+                sm.slot = 0;
+            __syncthreads();
+            for (int i = tid; i < n; i += kThreads) {
+                if (sm.ckey[i] > K) {
+                    const uint32_t sl = gt1 + static_cast<uint32_t>(atomicAdd(&sm.slot, 1));
+                    const int pos = sm.cpos[i];
+                    oidx[sl] = map ? map[pos] : pos;
+                    if (oval)
+                        oval[sl] = key_float(sm.ckey[i]);
+                }
+            }
+            __syncthreads();
+            const uint32_t eq_base = gt1 + static_cast<uint32_t>(sm.slot);
+            // ties at K: all, or the `need` lowest positions (radix select on positions)
+            uint32_t pmax = 0xFFFFFFFFu;
+            if (cnt_eq != need) {
+                uint32_t P = 0, need_p = need;
+                for (int lv = 0; lv < 3; ++lv) {
+                    const int hs = lv == 0 ? 21 : (lv == 1 ? 10 : 0);
+                    const int ws = lv == 2 ? 10 : 11;
+                    const uint32_t pm = lv == 0 ? 0u : (0xFFFFFFFFu << (hs + ws));
+                    for (int i = tid; i < kRBins; i += kThreads)
+                        sm.hist[i] = 0u;
+                    __syncthreads();
+                    for (int i = tid; i < n; i += kThreads) {
+                        const uint32_t up = static_cast<uint32_t>(sm.cpos[i]);
+                        if (sm.ckey[i] == K && (up & pm) == (P & pm))
+                            atomicAdd(&sm.hist[kRBins - 1 - ((up >> hs) & ((1u << ws) - 1u))], 1u);
+                    }
+                    __syncthreads();
+                    // bins mirrored: the largest mirrored bin is the smallest digit
+                    int b;
+                    uint32_t gt;
+                    reg_select_bin(sm, need_p, b, gt);
+                    need_p -= gt;
+                    P |= static_cast<uint32_t>(kRBins - 1 - b) << hs;
+                }
+                pmax = P;
+            }
+            if (tid == 0)
+                sm.slot = 0;
+            __syncthreads();
+            for (int i = tid; i < n; i += kThreads) {
+                const int pos = sm.cpos[i];
+                if (sm.ckey[i] == K && static_cast<uint32_t>(pos) <= pmax) {
+                    const uint32_t sl = eq_base + static_cast<uint32_t>(atomicAdd(&sm.slot, 1));
+                    oidx[sl] = map ? map[pos] : pos;
+                    if (oval)
+                        oval[sl] = key_float(K);
+                }
+            }
+            __syncthreads();
+            continue;
         }
         if (shift1 > 0) {
             // level 2: bits [shift2, shift1) of keys in the level-1 bin
