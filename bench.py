@@ -104,18 +104,24 @@ def source_hash(paths) -> str:
     return h.hexdigest()[:16]
 
 
+SCAN_SOURCES = ["shared_latent_key_cache_b300/csrc/score_tc.cu", "shared_latent_key_cache_b300/csrc/ptx.cuh",
+                "shared_latent_key_cache_b300/csrc/li_internal.cuh"]
+
+
 def ncu_traffic(workload: str):
-    """Per-launch DRAM bytes of the scan kernel from the committed ncu summary,
-    if it was taken on the current kernel source (else None)."""
-    p = os.path.join(ROOT, "profiles", "traffic.json")
+    """DRAM bytes (read + write) per launch of the scan kernel from the
+    committed ncu summary of this workload, if that capture was taken on the
+    current kernel sources (else None)."""
+    import re
+    p = os.path.join(ROOT, "profiles", f"decode_{workload}_kernels_full.md")
     if not os.path.exists(p):
         return None
-    with open(p) as f:
-        d = json.load(f)
-    e = d.get(workload)
-    if not e or e.get("source_hash") != source_hash(e.get("sources", [])):
+    text = open(p).read()
+    mh = re.search(r"scan_kernel_sources_sha256_16: ([0-9a-f]{16})", text)
+    mb = re.search(r"dram_bytes_per_launch: ([0-9]+)", text)
+    if not mh or not mb or mh.group(1) != source_hash(SCAN_SOURCES):
         return None
-    return e.get("dram_bytes_per_launch")
+    return int(mb.group(1))
 
 
 class L2Flush:

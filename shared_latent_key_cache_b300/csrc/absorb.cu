@@ -17,6 +17,7 @@
 #include <cuda_fp8.h>
 
 #include "li_internal.cuh"
+#include "ptx.cuh"
 
 namespace li {
 namespace {
@@ -66,6 +67,8 @@ __global__ void __launch_bounds__(kThreads) absorb_kernel(AbsorbParams p)
     __shared__ __align__(16) float qs[kKC][kQPad];
     __shared__ __align__(16) float Ds[kKC][kDPad];
 
+    griddep_wait();
+    griddep_launch_dependents();
     const int l = blockIdx.y;
     const int tid = threadIdx.x;
     const int ty = tid / 16, tx = tid % 16;
@@ -264,8 +267,7 @@ cudaError_t launch_absorb(const AbsorbParams &p, cudaStream_t s)
     if (gx > 0x7FFFFFFF || p.G > 65535 || p.r > kMaxR)
         return cudaErrorInvalidValue;
     dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(p.G));
-    absorb_kernel<<<grid, kThreads, 0, s>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(absorb_kernel, grid, dim3(kThreads), 0, s, p);
 }
 
 } // namespace li

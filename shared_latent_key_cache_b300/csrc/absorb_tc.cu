@@ -81,6 +81,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = tmem_base_s;
+    griddep_wait();
+    griddep_launch_dependents();
 
     bool ok = true;
     if (warp == 0) {
@@ -289,8 +291,8 @@ cudaError_t launch_absorb_tc(const AbsorbParams &p, cudaStream_t s)
     if (tiles > 0x7FFFFFFF)
         return cudaErrorInvalidValue;
     dim3 grid(static_cast<unsigned>(tiles), static_cast<unsigned>(p.G));
-    absorb_tc_kernel<<<grid, kThreads, smem, s>>>(tmQ, tmD, p, c, status);
-    return cudaGetLastError();
+    return launch_pdl(absorb_tc_kernel, grid, dim3(kThreads), static_cast<size_t>(smem), s, tmQ, tmD, p, c,
+                      status);
 }
 
 } // namespace li

@@ -4,6 +4,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 
 #include <cuda.h>           // CUtensorMap and the tensor-map encoder's types
 #include <cuda_runtime.h>
@@ -85,6 +86,28 @@ struct TopkParams {
     int *status;
 };
 cudaError_t launch_topk(const TopkParams &p, cudaStream_t s);
+
+// Launches `kern` on stream `s` with programmatic stream serialization: the
+// kernel may be scheduled while its predecessor in the stream finishes.  The
+// library's kernels execute griddepcontrol.wait (griddep_wait) before their
+// first global memory access, so only their set-up (shared memory, barriers,
+// tensor memory) overlaps the predecessor.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // Per-device status word (address of the __device__ variable on the current
 // device), or nullptr on failure.

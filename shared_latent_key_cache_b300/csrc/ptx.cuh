@@ -25,6 +25,25 @@ __device__ __forceinline__ uint64_t globaltimer_ns()
     return t;
 }
 
+// ------------------------------------------------- programmatic dependent launch
+
+// Wait until the grids this one depends on (its predecessor in the stream,
+// when launched with programmatic stream serialization) have completed and
+// their memory is visible.  A no-op for a kernel launched without it.  Every
+// kernel of this library executes it in every thread before its first global
+// memory access, so only set-up work overlaps the predecessor.
+__device__ __forceinline__ void griddep_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Let the next kernel in the stream be scheduled now (it still waits for this
+// grid's completion before touching memory).
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ mbarrier
 
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)

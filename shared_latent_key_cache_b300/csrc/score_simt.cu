@@ -17,6 +17,7 @@
 #include <atomic>
 
 #include "li_internal.cuh"
+#include "ptx.cuh"
 
 namespace li {
 namespace {
@@ -36,6 +37,8 @@ __device__ __forceinline__ float decode(const void *p, int dtype, int64_t i)
 __global__ void __launch_bounds__(kTok) score_simt_kernel(const ScoreParams p)
 {
     extern __shared__ float sm[];
+    griddep_wait();
+    griddep_launch_dependents();
     const int N = p.Gs * p.H;
     const int rp = p.r + 1;
     float *qs = sm;                     // [N][r]
@@ -130,8 +133,8 @@ cudaError_t launch_score_simt(const ScoreParams &p, cudaStream_t s)
         return cudaSuccess;
     if (gy > 65535)
         return cudaErrorInvalidValue;
-    score_simt_kernel<<<dim3(gx, static_cast<unsigned>(gy)), kTok, smem, s>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(score_simt_kernel, dim3(gx, static_cast<unsigned>(gy)), dim3(kTok),
+                      static_cast<size_t>(smem), s, p);
 }
 
 } // namespace li

@@ -253,6 +253,8 @@ __global__ void __launch_bounds__(Roles<kGather>::kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = misc->tmem_base;
+    griddep_wait();
+    griddep_launch_dependents();
 
     // Issues the query operand of row bt into buffer (nb % nbuf); returns false
     // on abort.  Called by a whole warp; lane 0 issues the copies.
@@ -748,8 +750,8 @@ cudaError_t launch_t(const CUtensorMap &tmA, const CUtensorMap &tmB, const Score
         grid = c.U;
     if (grid <= 0)
         return cudaSuccess;
-    kern<<<static_cast<unsigned>(grid), Roles<kGather>::kThreads, smem_bytes, s>>>(tmA, tmB, p, c);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(Roles<kGather>::kThreads),
+                      static_cast<size_t>(smem_bytes), s, tmA, tmB, p, c);
 }
 
 template <bool kFP8, bool kGather, bool kBeta>

@@ -35,6 +35,7 @@
 #include <cstdint>
 
 #include "li_internal.cuh"
+#include "ptx.cuh"
 
 namespace li {
 namespace {
@@ -325,6 +326,8 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p)
     extern __shared__ __align__(16) uint8_t smraw[];
     TopkSmem &sm = *reinterpret_cast<TopkSmem *>(smraw);
     const int tid = threadIdx.x;
+    griddep_wait();
+    griddep_launch_dependents();
 
     for (int64_t row = blockIdx.x; row < p.rows; row += gridDim.x) {
         const float *src = p.scores + row * p.in_stride;
@@ -687,6 +690,8 @@ __global__ void __launch_bounds__(kThreads, 1) topk_reg_kernel(const TopkParams 
 {
     __shared__ RegSmem sm;
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    griddep_wait();
+    griddep_launch_dependents();
 
     for (int64_t row = blockIdx.x; row < p.rows; row += gridDim.x) {
         const float *src = p.scores + row * p.in_stride;
@@ -1032,10 +1037,8 @@ cudaError_t launch_topk(const TopkParams &p, cudaStream_t s)
     }
     const int64_t grid = p.rows < 0x7FFFFFFF ? p.rows : 0x7FFFFFFF;
     if (p.L_row <= kRegRow)
-        topk_reg_kernel<<<static_cast<unsigned>(grid), kThreads, 0, s>>>(p);
-    else
-        topk_kernel<<<static_cast<unsigned>(grid), kThreads, smem, s>>>(p);
-    return cudaGetLastError();
+        return launch_pdl(topk_reg_kernel, dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, s, p);
+    return launch_pdl(topk_kernel, dim3(static_cast<unsigned>(grid)), dim3(kThreads), static_cast<size_t>(smem), s, p);
 }
 
 } // namespace li
