@@ -30,13 +30,15 @@
 //                   candidates): each thread copies two tile rows of gathered
 //                   latent with 16-byte cp.async into the swizzled layout TMA
 //                   would write, several tiles in flight per thread
-//   16 warps        epilogue, four per TMEM lane quarter (warp % 4), each
-//                   owning 64 (or H when H > 64) accumulator columns, i.e. one
-//                   layer at H = 64: both 32-column TMEM loads in flight, the
-//                   accumulator released as soon as they land, then ReLU,
-//                   weighted head sums with packed fp32 FMA, per-token scale
-//                   (prefetched one tile ahead) and one coalesced store per
-//                   layer
+//   8 warps         epilogue, two per TMEM lane quarter (warp % 4), each
+//                   owning 128 accumulator columns (two layers at H = 64): all
+//                   four 32-column TMEM loads in flight, the accumulator
+//                   released as soon as they land, then ReLU, weighted head
+//                   sums with packed fp32 FMA, per-token scale (prefetched one
+//                   tile ahead) and one coalesced store per layer.  (Sixteen
+//                   warps of 64 columns spent more issue slots on per-tile
+//                   bookkeeping than on the arithmetic: the epilogue's issue
+//                   rate, not HBM, set the tile period.)
 // The two TMEM accumulators (2 x 256 columns) are double-buffered so the
 // epilogue of tile i overlaps the MMAs of tile i+1 and the loads of the tiles
 // after it.
@@ -59,7 +61,7 @@ namespace {
 constexpr int kTileM = 128;
 constexpr int kChunkElems = 64;
 constexpr int kMaxDev = 64;
-constexpr int kEpiWarps = 16;
+constexpr int kEpiWarps = 8;
 constexpr int kTmemCols = 512;          // two accumulators of 256 columns
 constexpr int kAccStride = 256;
 constexpr int kConstCap = 1024;         // active epilogue warps x columns per warp
@@ -508,7 +510,7 @@ __global__ void __launch_bounds__(Roles<kGather>::kThreads, 1)
         __syncwarp();
     } else if (warp >= R::kEpiWarp0) {
         // ------------------------------------------------------------ epilogue
-        const int e = warp - R::kEpiWarp0;          // 0..15
+        const int e = warp - R::kEpiWarp0;          // 0..7
         const int quarter = warp & 3;               // TMEM lane quarter
         const int c0 = (e >> 2) * c.cw;             // first accumulator column
         if (c0 < c.N) {
@@ -577,7 +579,9 @@ __global__ void __launch_bounds__(Roles<kGather>::kThreads, 1)
                             sq[j] = sv;
                             bq[j] = p.beta[wrow + j];
                         } else {
-                            wq[j] = wv * sv;
+                            // columns 2 and 3 of every 4 take the ReLU as (x + |x|) / 2
+                            // on the FMA pipe (see the epilogue): their weight is halved
+                            wq[j] = (j & 3) >= 2 ? 0.5f * (wv * sv) : wv * sv;
                         }
                     }
                     __syncwarp();
@@ -598,7 +602,6 @@ __global__ void __launch_bounds__(Roles<kGather>::kThreads, 1)
                     if (valid && lay < nlay)
                         out[static_cast<int64_t>(lay) * p.L_out] = u;
                 };
-                float2 a0 = make_float2(0.f, 0.f), a1 = a0, a2 = a0, a3 = a0;
                 // 32 accumulator columns starting at column `col` (relative to
                 // c0) into the running sums (x, y)
                 auto chunk = [&](const uint32_t(&v)[32], int col, float2 &x, float2 &y) {
@@ -620,12 +623,17 @@ __global__ void __launch_bounds__(Roles<kGather>::kThreads, 1)
 #pragma unroll
                         for (int j = 0; j < 8; ++j) {
                             const float4 ww = w4[j];
+                            // ReLU split between the ALU pipe (fmax, columns 0-1) and
+                            // the FMA pipe (x + |x| = 2 ReLU(x) against a halved
+                            // weight, columns 2-3; both scalings by 2 are exact), so
+                            // that neither pipe carries all of it
+                            const float c2 = __uint_as_float(v[4 * j + 2]);
+                            const float c3 = __uint_as_float(v[4 * j + 3]);
                             x = __ffma2_rn(make_float2(ww.x, ww.y),
                                            make_float2(fmaxf(__uint_as_float(v[4 * j]), 0.f),
                                                        fmaxf(__uint_as_float(v[4 * j + 1]), 0.f)), x);
                             y = __ffma2_rn(make_float2(ww.z, ww.w),
-                                           make_float2(fmaxf(__uint_as_float(v[4 * j + 2]), 0.f),
-                                                       fmaxf(__uint_as_float(v[4 * j + 3]), 0.f)), y);
+                                           make_float2(c2 + fabsf(c2), c3 + fabsf(c3)), y);
                             if (kH == 16 && (j == 3 || j == 7)) {
                                 finish((col + 4 * j) / 16, (x.x + x.y) + (y.x + y.y));
                                 x = make_float2(0.f, 0.f);
@@ -639,34 +647,44 @@ __global__ void __launch_bounds__(Roles<kGather>::kThreads, 1)
                         y = x;
                     }
                 };
-                for (int cb = 0; cb < ncols; cb += 64) {
-                    uint32_t va[32], vb[32];
-                    tmem_ld32(tacc + static_cast<uint32_t>(cb), va);
-                    tmem_ld32(tacc + static_cast<uint32_t>(cb + 32), vb);
-                    tmem_ld_wait32(va);
-                    tmem_regs_ready(vb);
-                    if (cb + 64 >= ncols) {
-                        // The whole block is in registers: release the accumulator.
-                        // A relaxed arrival: a release would first wait for this
-                        // warp's outstanding global loads and stores (the next
-                        // tile's scale prefetch, the last tile's scores), which
-                        // holds the accumulator, and so the MMAs, ~1 us longer.
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0)
-                            mbar_arrive_relaxed(&bars->tmem_empty[acc]);
-                    }
-                    chunk(va, cb, a0, a1);
-                    chunk(vb, cb + 32, a2, a3);
-                    if (kH >= 64 && ((cb + 64) % kH) == 0) {
-                        finish((cb + 63) / kH, ((a0.x + a0.y) + (a1.x + a1.y)) +
-                                                   ((a2.x + a2.y) + (a3.x + a3.y)));
-                        a0 = make_float2(0.f, 0.f);
-                        a1 = a0;
-                        a2 = a0;
-                        a3 = a0;
-                    }
+                // All of the warp's (<= 128) columns in flight at once; the
+                // accumulator is released as soon as they have landed.
+                uint32_t va[32], vb[32], vc[32], vd[32];
+                tmem_ld32(tacc, va);
+                if (ncols > 32)
+                    tmem_ld32(tacc + 32u, vb);
+                if (ncols > 64)
+                    tmem_ld32(tacc + 64u, vc);
+                if (ncols > 96)
+                    tmem_ld32(tacc + 96u, vd);
+                tmem_ld_wait32(va);
+                tmem_regs_ready(vb);
+                tmem_regs_ready(vc);
+                tmem_regs_ready(vd);
+                // A relaxed arrival: a release would first wait for this warp's
+                // outstanding global loads and stores (the next tile's scale
+                // prefetch, the last tile's scores).
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive_relaxed(&bars->tmem_empty[acc]);
+                float2 x0 = make_float2(0.f, 0.f), y0 = x0, x1 = x0, y1 = x0;
+                chunk(va, 0, x0, y0);
+                if (ncols > 32)
+                    chunk(vb, 32, x0, y0);
+                if (kH == 64) {
+                    finish(0, (x0.x + x0.y) + (y0.x + y0.y));
+                    x0 = make_float2(0.f, 0.f);
+                    y0 = x0;
                 }
+                if (ncols > 64)
+                    chunk(vc, 64, x1, y1);
+                if (ncols > 96)
+                    chunk(vd, 96, x1, y1);
+                if (kH == 64 && ncols > 64)
+                    finish(1, (x1.x + x1.y) + (y1.x + y1.y));
+                if (kH == 128)
+                    finish(0, ((x0.x + x0.y) + (y0.x + y0.y)) + ((x1.x + x1.y) + (y1.x + y1.y)));
                 w.next(p, c.NT);
                 sc_cur = sc_next;
                 tok1 = tok2;
@@ -718,7 +736,7 @@ bool make_config(const ScoreParams &p, bool fp8, TcConfig &c, int &smem_bytes)
     // one CTA per SM: a second CTA would only queue on the TMEM allocation
     if (smem_bytes < 116 * 1024)
         smem_bytes = 116 * 1024;
-    c.cw = p.H >= 64 ? p.H : 64;
+    c.cw = 128;                           // accumulator columns per epilogue warp
     c.nepi = 4 * ((c.N + c.cw - 1) / c.cw);
     c.gdepth = stages - 1 < 3 ? stages - 1 : 3;
     const int Lrow = p.gather_idx ? p.L_out : p.L_lat;
