@@ -195,6 +195,18 @@ int li_native_score(const void *keys, int key_t, const float *key_scale,
                     int B, int H, int d, int L, float *scores, void *stream);
 
 /*
+ * Test hook for the device-side watchdog (no counterpart on the pages).
+ * Launches one CTA that allocates tensor memory and waits, with the bounded
+ * mbarrier wait every kernel of this library uses, on a barrier that nothing
+ * ever arrives on.  After `limit_us` microseconds (1 ... 1,000,000) the wait
+ * gives up and latches LI_ERR_TIMEOUT in the device status word; the CTA
+ * frees its tensor memory and exits, leaving the context usable.  The next
+ * li_device_status() returns LI_ERR_TIMEOUT.  Returns LI_ERR_INVALID_ARG for
+ * a limit out of range, LI_ERR_CUDA if the launch fails.
+ */
+int li_selftest_wait_timeout(unsigned int limit_us, void *stream);
+
+/*
  * Synchronises `stream`, then returns and clears the calling device's status
  * word: LI_OK, or the first device-side error latched since the last call
  * (LI_ERR_TIMEOUT, LI_ERR_DEVICE_BOUNDS), or LI_ERR_CUDA if the

@@ -23,7 +23,7 @@ __all__ = [
     "LI_F32", "LI_BF16", "LI_FP8_E4M3", "LiError", "lib", "library_path",
     "li_version", "li_status_string", "li_absorb_queries", "li_score_group", "li_topk",
     "li_hs_workspace_size", "li_hs_select", "li_hs_select_noalloc", "li_native_score",
-    "li_device_status",
+    "li_device_status", "li_selftest_wait_timeout",
     "absorb_queries", "score_group", "topk", "hs_select", "native_score", "device_status",
 ]
 
@@ -59,8 +59,10 @@ def _load():
     L.li_native_score.argtypes = [P, I, P, P, I, P, P, I, I, I, I, P, P]
     L.li_hs_select_noalloc.argtypes = [P, I, P, P, I, P, P, P, I, I, I, I, I, I, I, P, P, P]
     L.li_device_status.argtypes = [P]
+    L.li_selftest_wait_timeout.argtypes = [ctypes.c_uint, P]
     for f in ("li_absorb_queries", "li_score_group", "li_topk", "li_hs_select",
-              "li_native_score", "li_device_status", "li_hs_select_noalloc"):
+              "li_native_score", "li_device_status", "li_hs_select_noalloc",
+              "li_selftest_wait_timeout"):
         getattr(L, f).restype = I
     return L
 
@@ -186,6 +188,11 @@ def li_native_score(keys, key_scale, q, q_scale, w, scores, stream=None) -> int:
 
 def li_device_status(stream=None) -> int:
     return _lib.li_device_status(_stream(stream))
+
+
+def li_selftest_wait_timeout(limit_us: int, stream=None) -> int:
+    """Launch the watchdog test kernel (a bounded wait that is never satisfied)."""
+    return _lib.li_selftest_wait_timeout(int(limit_us), _stream(stream))
 
 
 # ------------------------------------------------------- allocating helpers

@@ -50,6 +50,11 @@ def test_exports_are_c_symbols(li):
         getattr(lib, n)   # unmangled lookup succeeds only for extern "C" symbols
 
 
+def test_selftest_limit_checked_before_any_cuda_call(L):
+    for bad in (0, 1_000_001, 4_000_000_000):
+        assert L.li_selftest_wait_timeout(bad, None) == -1
+
+
 def test_version_and_status_strings(L):
     assert L.li_version() >= 100
     for s in (0, -1, -2, -3, -4, -5, -6, -7):
