@@ -592,6 +592,7 @@ constexpr int kRegRow = kRegPer * kThreads;
 constexpr int kRBins = 2048;
 
 constexpr int kRCap = 4096;       // candidate list (keys in the threshold bin)
+constexpr int kRankMax = 256;     // lists up to this long are ranked by counting
 
 struct RegSmem {
     uint32_t hist[kRBins];
@@ -725,16 +726,28 @@ __global__ void __launch_bounds__(kThreads, 1) topk_reg_kernel(const TopkParams 
         // ---- load: element e of this thread is at position 4 (tid + 1024 (e / 4)) + e % 4
         uint32_t key[kRegPer];
         const bool al16 = (reinterpret_cast<uintptr_t>(src) & 15u) == 0;
+        if (al16 && (p.L_row & 3) == 0) {
+            // All eight 16-byte loads of the thread in flight at once: a load is
+            // skipped only past the row's storage (p.L_row), positions in
+            // [V, p.L_row) are read and then ignored through valid().
+            const float4 *r4 = reinterpret_cast<const float4 *>(src);
+            float4 v[kRegPer / 4];
 #pragma unroll
-        for (int i = 0; i < kRegPer / 4; ++i) {
-            const int pos = 4 * (tid + kThreads * i);
-            if (al16 && pos + 3 < V) {
-                const float4 v = __ldg(reinterpret_cast<const float4 *>(src + pos));
-                key[4 * i] = float_key(v.x);
-                key[4 * i + 1] = float_key(v.y);
-                key[4 * i + 2] = float_key(v.z);
-                key[4 * i + 3] = float_key(v.w);
-            } else {
+            for (int i = 0; i < kRegPer / 4; ++i) {
+                const int q = tid + kThreads * i;
+                v[i] = 4 * q < p.L_row ? __ldg(r4 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int i = 0; i < kRegPer / 4; ++i) {
+                key[4 * i] = float_key(v[i].x);
+                key[4 * i + 1] = float_key(v[i].y);
+                key[4 * i + 2] = float_key(v[i].z);
+                key[4 * i + 3] = float_key(v[i].w);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < kRegPer / 4; ++i) {
+                const int pos = 4 * (tid + kThreads * i);
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
                     key[4 * i + j] = pos + j < V ? float_key(__ldg(src + pos + j)) : 0u;
@@ -802,38 +815,90 @@ __global__ void __launch_bounds__(kThreads, 1) topk_reg_kernel(const TopkParams 
             // ---- usual case: keys above the level-1 bin are selected now, the
             // bin's keys move to a shared-memory list and the remaining digits
             // and the ties are resolved on that list only
-            const uint32_t b1 = T >> shift1;
             const uint32_t gt1 = static_cast<uint32_t>(nsel) - need;
+            // offsets key - kmin inside the threshold bin: [lo_off, hi_off]
+            // (T + 2^shift1 - 1 stays below 2^nbits, so it does not wrap)
+            const uint32_t lo_off = T;
+            const uint32_t hi_off = T + ((1u << shift1) - 1u);
             uint32_t n_sure = 0, n_cand = 0;
 #pragma unroll
             for (int e = 0; e < kRegPer; ++e) {
                 if (valid(e)) {
-                    const uint32_t bn = (key[e] - kmin) >> shift1;
-                    n_sure += bn > b1 ? 1u : 0u;
-                    n_cand += bn == b1 ? 1u : 0u;
+                    const uint32_t o = key[e] - kmin;
+                    n_sure += o > hi_off ? 1u : 0u;
+                    n_cand += o >= lo_off ? 1u : 0u;
                 }
             }
+            n_cand -= n_sure;
             uint32_t so = warp_reserve(&sm.out_cnt, n_sure);
             uint32_t co = warp_reserve(&sm.cand_cnt, n_cand);
+            if (map == nullptr && oval == nullptr) {
 #pragma unroll
-            for (int e = 0; e < kRegPer; ++e) {
-                if (valid(e)) {
-                    const uint32_t bn = (key[e] - kmin) >> shift1;
-                    const int pos = 4 * (tid + kThreads * (e >> 2)) + (e & 3);
-                    if (bn > b1) {
-                        oidx[so] = map ? map[pos] : pos;
-                        if (oval)
-                            oval[so] = key_float(key[e]);
-                        ++so;
-                    } else if (bn == b1) {
-                        sm.ckey[co] = key[e];
-                        sm.cpos[co] = pos;
-                        ++co;
+                for (int e = 0; e < kRegPer; ++e) {
+                    const uint32_t o = key[e] - kmin;
+                    if (valid(e) && o >= lo_off) {
+                        const int pos = 4 * (tid + kThreads * (e >> 2)) + (e & 3);
+                        if (o > hi_off) {
+                            oidx[so] = pos;
+                            ++so;
+                        } else {
+                            sm.ckey[co] = key[e];
+                            sm.cpos[co] = pos;
+                            ++co;
+                        }
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < kRegPer; ++e) {
+                    const uint32_t o = key[e] - kmin;
+                    if (valid(e) && o >= lo_off) {
+                        const int pos = 4 * (tid + kThreads * (e >> 2)) + (e & 3);
+                        if (o > hi_off) {
+                            oidx[so] = map ? map[pos] : pos;
+                            if (oval)
+                                oval[so] = key_float(key[e]);
+                            ++so;
+                        } else {
+                            sm.ckey[co] = key[e];
+                            sm.cpos[co] = map ? map[pos] : pos;
+                            ++co;
+                        }
                     }
                 }
             }
             __syncthreads();
             const int n = static_cast<int>(cnt_eq);
+            if (n <= kRankMax) {
+                // Short list: each candidate's rank in (key desc, position asc)
+                // order is the number of candidates ahead of it, counted by four
+                // threads over a quarter of the list each; the `need` lowest
+                // ranks are taken, rank r into output slot gt1 + r.
+                const int c = tid >> 2, part = tid & 3;
+                const int per = (n + 3) >> 2;
+                uint32_t ahead = 0, ck = 0;
+                int cp = 0;
+                if (c < n) {
+                    ck = sm.ckey[c];
+                    cp = sm.cpos[c];
+                    const int j1 = min(n, (part + 1) * per);
+                    for (int j = part * per; j < j1; ++j) {
+                        const uint32_t kj = sm.ckey[j];
+                        const int pj = sm.cpos[j];
+                        ahead += (kj > ck || (kj == ck && pj < cp)) ? 1u : 0u;
+                    }
+                }
+                ahead += __shfl_xor_sync(0xffffffffu, ahead, 1);
+                ahead += __shfl_xor_sync(0xffffffffu, ahead, 2);
+                if (c < n && part == 0 && ahead < need) {
+                    const uint32_t sl = gt1 + ahead;
+                    oidx[sl] = cp;
+                    if (oval)
+                        oval[sl] = key_float(ck);
+                }
+                __syncthreads();
+                continue;
+            }
             for (int level = 0; level < 2; ++level) {
                 const int hs = level == 0 ? shift1 : shift2;
                 const int ls = level == 0 ? shift2 : 0;
@@ -864,8 +929,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_reg_kernel(const TopkParams 
             for (int i = tid; i < n; i += kThreads) {
                 if (sm.ckey[i] > K) {
                     const uint32_t sl = gt1 + static_cast<uint32_t>(atomicAdd(&sm.slot, 1));
-                    const int pos = sm.cpos[i];
-                    oidx[sl] = map ? map[pos] : pos;
+                    oidx[sl] = sm.cpos[i];
                     if (oval)
                         oval[sl] = key_float(sm.ckey[i]);
                 }
@@ -905,7 +969,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_reg_kernel(const TopkParams 
                 const int pos = sm.cpos[i];
                 if (sm.ckey[i] == K && static_cast<uint32_t>(pos) <= pmax) {
                     const uint32_t sl = eq_base + static_cast<uint32_t>(atomicAdd(&sm.slot, 1));
-                    oidx[sl] = map ? map[pos] : pos;
+                    oidx[sl] = pos;
                     if (oval)
                         oval[sl] = key_float(K);
                 }
@@ -982,6 +1046,49 @@ __global__ void __launch_bounds__(kThreads, 1) topk_reg_kernel(const TopkParams 
                     oidx[s2] = map ? map[pos] : pos;
                     if (oval)
                         oval[s2] = key_float(K);
+                }
+            }
+        } else if (map != nullptr) {
+            // positions of this row index a candidate list (map): ties are
+            // taken by lowest mapped position, found by a radix select on
+            // the mapped positions of the tied keys (the map's entries are
+            // distinct), then emitted in any order
+            uint32_t P = 0, need_p = need;
+            for (int lv = 0; lv < 3; ++lv) {
+                const int hs = lv == 0 ? 21 : (lv == 1 ? 10 : 0);
+                const int ws = lv == 2 ? 10 : 11;
+                const uint32_t pm = lv == 0 ? 0u : (0xFFFFFFFFu << (hs + ws));
+                for (int i = tid; i < kRBins; i += kThreads)
+                    sm.hist[i] = 0u;
+                __syncthreads();
+#pragma unroll
+                for (int e = 0; e < kRegPer; ++e) {
+                    if (valid(e) && key[e] == K) {
+                        const uint32_t up = static_cast<uint32_t>(map[4 * (tid + kThreads * (e >> 2)) + (e & 3)]);
+                        if ((up & pm) == (P & pm))
+                            atomicAdd(&sm.hist[kRBins - 1 - ((up >> hs) & ((1u << ws) - 1u))], 1u);
+                    }
+                }
+                __syncthreads();
+                int b;
+                uint32_t gt;
+                reg_select_bin(sm, need_p, b, gt);
+                need_p -= gt;
+                P |= static_cast<uint32_t>(kRBins - 1 - b) << hs;
+            }
+            if (tid == 0)
+                sm.slot = 0;
+            __syncthreads();
+#pragma unroll
+            for (int e = 0; e < kRegPer; ++e) {
+                if (valid(e) && key[e] == K) {
+                    const int up = map[4 * (tid + kThreads * (e >> 2)) + (e & 3)];
+                    if (static_cast<uint32_t>(up) <= P) {
+                        const int s2 = static_cast<int>(sure) + atomicAdd(&sm.slot, 1);
+                        oidx[s2] = up;
+                        if (oval)
+                            oval[s2] = key_float(K);
+                    }
                 }
             }
         } else {

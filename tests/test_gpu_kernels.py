@@ -176,6 +176,23 @@ def test_topk_ties_take_lowest_positions(li, orc):
         exact_sets_equal(gi, oi)
 
 
+def test_topk_short_threshold_list_with_ties(li, orc):
+    """Decode-length rows whose threshold bin holds a short candidate list with
+    exact ties at the k-th score: the list is ranked by counting, ties by position."""
+    g = torch.Generator().manual_seed(21)
+    s = torch.randn(6, 32768, generator=g) * 5 + 10
+    for r in range(6):
+        v = s[r].sort(descending=True).values[2047 - 3 * r]
+        pos = torch.randperm(32768, generator=g)[:2 + 7 * r]
+        s[r, pos] = v
+    s[5, 100:140] = s[5].max()                       # ties among the sure keys too
+    for k in (1, 2000, 2048, 2100):
+        gi, gv = _topk_gpu(li, s, k)
+        oi, ov = orc.topk(s.double().numpy(), k)
+        exact_sets_equal(gi, oi)
+        np.testing.assert_array_equal(np.sort(gv, axis=1), np.sort(ov.astype(np.float32), axis=1))
+
+
 def test_topk_threshold_bin_overflows_shared_memory(li, orc):
     """Scores sharing their top 12 key bits (one exponent, same 3 mantissa bits) force the
     re-read path; a narrower cluster forces the second-digit re-read too."""
@@ -306,6 +323,42 @@ def test_hs_budget_equal_k_gives_candidates(li, orc):
     for b in range(2):
         for l in range(w.G):
             assert set(gi[b, l].tolist()) == set(c[b].tolist())
+
+
+def _hs_exact_vs_scan(li, orc, lat, sc, x, m, k):
+    """HS against the oracle's selection on the scan's own fp32 scores (the HS
+    kernels score with the same arithmetic), so tied scores are exactly tied."""
+    w = x["spec"]
+    qa, qs = li.absorb_queries(_dev(x["q"]), _dev(x["D"]), "fp8")
+    s = li.score_group(_dev(lat), _dev(sc), qa, qs, _dev(x["w"]))
+    cand, idx = li.hs_select(_dev(lat), _dev(sc), qa, qs, _dev(x["w"]), m, k)
+    _sync_ok(li)
+    oc, oi = orc.hs(s[:, 0].cpu().double().numpy(), m, k)
+    exact_sets_equal(cand.cpu().numpy(), oc)
+    exact_sets_equal(idx.cpu().numpy(), oi)
+
+
+def test_hs_ties_taken_by_lowest_token_position(li, orc):
+    """Every latent row appears twice, so every score is tied with another
+    token's: anchor candidates and follower selections must take the lower
+    token positions (the candidate list's own order is arbitrary)."""
+    w = li_inputs.spec("fp8_128k_hs", B=2, L=4000, m=600, k=150)
+    x = li_inputs.make_workload(w, seed=8)
+    lat, sc = x["latent"].clone(), x["lat_scale"].clone()
+    lat[:, 2000:] = lat[:, :2000]
+    sc[:, 2000:] = sc[:, :2000]
+    _hs_exact_vs_scan(li, orc, lat, sc, x, 600, 150)
+
+
+def test_hs_many_ties_at_the_follower_threshold(li, orc):
+    """Zero latent rows score exactly 0 in every layer: with k above the number
+    of positive scores, thousands of candidates tie at the threshold and the
+    lowest token positions among them are taken."""
+    w = li_inputs.spec("fp8_128k_hs", B=1, L=12000, m=8192, k=5000)
+    x = li_inputs.make_workload(w, seed=9)
+    lat, sc = x["latent"].clone(), x["lat_scale"].clone()
+    lat[:, 3000:] = 0
+    _hs_exact_vs_scan(li, orc, lat, sc, x, 8192, 5000)
 
 
 @pytest.mark.parametrize("d,r", [(40, 64), (36, 100), (128, 256)])
