@@ -286,6 +286,9 @@ def run_ours(a, w):
     if x["q_pos"] is not None:
         vl = (x["q_pos"] + 1).repeat_interleave(G).contiguous()
     flush = L2Flush(dev)
+    # top-k workspace for the two-pass selection of rows longer than 32,768
+    tws_n = li.li_topk_workspace_size(B * T * G, L, k) if vl is None else 0
+    tws = torch.empty(tws_n, dtype=torch.uint8, device=dev) if tws_n > 0 else None
 
     def chk(st, what):
         if st != 0:
@@ -301,7 +304,7 @@ def run_ours(a, w):
                               q_pos=x["q_pos"], stream=stream), "score")
         if ev is not None:
             ev[2].record(stream)
-        chk(li.li_topk(scores, k, idx, None, vl, stream), "topk")
+        chk(li.li_topk(scores, k, idx, None, vl, tws, stream), "topk")
         if ev is not None:
             ev[3].record(stream)
 
@@ -380,7 +383,8 @@ def run_ours(a, w):
                       "q_abs": torch.empty_like(q_abs),
                       "q_scale": torch.empty_like(q_scale) if q_scale is not None else None,
                       "scores": torch.empty_like(scores), "idx": torch.empty_like(idx),
-                      "idx_h": torch.empty(idx.shape, dtype=torch.int32).pin_memory()})
+                      "idx_h": torch.empty(idx.shape, dtype=torch.int32).pin_memory(),
+                      "tws": torch.empty_like(tws) if tws is not None else None})
 
     def e2e_step(i):
         st, sl = streams[i % NS], slots[i % NS]
@@ -390,7 +394,7 @@ def run_ours(a, w):
             chk(li.li_absorb_queries(sl["q"], x["D"], sl["q_abs"], sl["q_scale"], st), "absorb")
             chk(li.li_score_group(x["latent"], x["lat_scale"], sl["q_abs"], sl["q_scale"], sl["w"],
                                   sl["scores"], q_pos=x["q_pos"], stream=st), "score")
-            chk(li.li_topk(sl["scores"], k, sl["idx"], None, vl, st), "topk")
+            chk(li.li_topk(sl["scores"], k, sl["idx"], None, vl, sl["tws"], st), "topk")
             sl["idx_h"].copy_(sl["idx"], non_blocking=True)
 
     for i in range(2 * NS):                       # warm the streams
@@ -535,6 +539,8 @@ def side_timings(a, w, x, q_abs, q_scale, li, stream, flush, dev):
         wls = [x["w"][:, 0, l].contiguous() for l in range(G)]
         ns = torch.empty(B, L, dtype=torch.float32, device=dev)
         nidx = torch.empty(B, k, dtype=torch.int32, device=dev)
+        nws_n = li.li_topk_workspace_size(B, L, k)
+        nws = torch.empty(nws_n, dtype=torch.uint8, device=dev) if nws_n > 0 else None
 
         def native(with_topk=True):
             for l in range(G):
@@ -542,7 +548,7 @@ def side_timings(a, w, x, q_abs, q_scale, li, stream, flush, dev):
                 st |= li.li_native_score(x["keys"][l], x["key_scale"][l], q8.view(B, H, d),
                                          qs8.view(B, H), wls[l], ns, stream)
                 if with_topk:
-                    st |= li.li_topk(ns, k, nidx, None, None, stream)
+                    st |= li.li_topk(ns, k, nidx, None, None, nws, stream)
                 assert st == 0
         n_us = timeit(lambda: native(True))
         n_scan_us = timeit(lambda: native(False))

@@ -107,6 +107,13 @@ int li_score_group(const void *latent, int lat_t, const float *lat_scale,
                    float *scores, void *stream);
 
 /*
+ * Workspace bytes li_topk can use for these sizes: non-zero when the rows are
+ * longer than 32,768 scores and ceil(L / 32,768) * k <= 32,768 (for k = 2048,
+ * L up to 524,288; for k = 8192, L up to 131,072).
+ */
+size_t li_topk_workspace_size(int64_t rows, int L, int k);
+
+/*
  * Per-row top-k (summary page, TopK after eq. (8)): for each of `rows` score
  * rows of length L, the indices of the min(k, V) largest scores over the
  * valid prefix [0, V), V = valid_len[row] (NULL: V = L; values are clamped to
@@ -117,10 +124,16 @@ int li_score_group(const void *latent, int lat_t, const float *lat_scale,
  *   scores [rows][L] fp32; idx [rows][k] int32 out (set in unspecified order,
  *   slots past min(k, V) hold -1); vals [rows][k] fp32 out or NULL (the score
  *   of each selected index, -inf in padded slots).
- * Limits: 1 <= k <= 65536, L < 2^31.
+ *   ws     optional device workspace (16-byte aligned) of ws_bytes; with at
+ *          least li_topk_workspace_size(rows, L, k) bytes, rows longer than
+ *          32,768 and valid_len == NULL are selected in two passes (the exact
+ *          top-k of each 32,768-score segment, then of the segments'
+ *          candidates, ties by position) with more parallelism.  The result
+ *          is the same with or without it; NULL / too small = one pass.
+ * Limits: 1 <= k <= 2^30, L < 2^31.
  */
 int li_topk(const float *scores, int64_t rows, int L, const int32_t *valid_len, int k,
-            int32_t *idx, float *vals, void *stream);
+            int32_t *idx, float *vals, void *ws, size_t ws_bytes, void *stream);
 
 /* Workspace bytes li_hs_select needs for these sizes. */
 size_t li_hs_workspace_size(int B, int G, int L, int m, int k);
@@ -161,7 +174,7 @@ int li_hs_select(const void *latent, int lat_t, const float *lat_scale,
  * bytes; every GPU that loads the library holds it until the process exits).
  * Sizes whose li_hs_workspace_size(B, G, L, m, k) exceeds 8 MiB are rejected
  * with LI_ERR_WORKSPACE before anything runs (B = 8, L = 131072, m = 8192,
- * G = 4 needs 5 MiB).  The call allocates nothing.
+ * G = 4 needs 7 MiB).  The call allocates nothing.
  *  - The first call on a device, made with that device current, looks up the
  *    array's device address (cudaGetSymbolAddress) and caches it; make that
  *    first call before any stream capture.

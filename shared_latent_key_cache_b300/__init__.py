@@ -22,6 +22,7 @@ import torch
 __all__ = [
     "LI_F32", "LI_BF16", "LI_FP8_E4M3", "LiError", "lib", "library_path",
     "li_version", "li_status_string", "li_absorb_queries", "li_score_group", "li_topk",
+    "li_topk_workspace_size",
     "li_hs_workspace_size", "li_hs_select", "li_hs_select_noalloc", "li_native_score",
     "li_device_status", "li_selftest_wait_timeout",
     "absorb_queries", "score_group", "topk", "hs_select", "native_score", "device_status",
@@ -52,7 +53,9 @@ def _load():
     L.li_status_string.restype = ctypes.c_char_p
     L.li_absorb_queries.argtypes = [P, I, P, I, I, I, I, I, I, I, P, I, P, P]
     L.li_score_group.argtypes = [P, I, P, P, I, P, P, P, P, I, I, I, I, I, I, P, P]
-    L.li_topk.argtypes = [P, I64, I, P, I, P, P, P]
+    L.li_topk.argtypes = [P, I64, I, P, I, P, P, P, S, P]
+    L.li_topk_workspace_size.argtypes = [I64, I, I]
+    L.li_topk_workspace_size.restype = S
     L.li_hs_workspace_size.argtypes = [I, I, I, I, I]
     L.li_hs_workspace_size.restype = S
     L.li_hs_select.argtypes = [P, I, P, P, I, P, P, P, I, I, I, I, I, I, I, P, P, P, S, P]
@@ -140,11 +143,16 @@ def li_score_group(latent, lat_scale, q_abs, q_abs_scale, w, scores, beta=None, 
         _stream(stream))
 
 
-def li_topk(scores, k: int, idx, vals=None, valid_len=None, stream=None) -> int:
-    """scores [..., L] -> idx [..., k] int32 (+ vals [..., k])."""
+def li_topk_workspace_size(rows: int, L: int, k: int) -> int:
+    return _lib.li_topk_workspace_size(rows, L, k)
+
+
+def li_topk(scores, k: int, idx, vals=None, valid_len=None, ws=None, stream=None) -> int:
+    """scores [..., L] -> idx [..., k] int32 (+ vals [..., k]); ws: optional uint8 workspace."""
     L = scores.shape[-1]
     rows = scores.numel() // L if L else 0
     return _lib.li_topk(_ptr(scores), rows, L, _ptr(valid_len), k, _ptr(idx), _ptr(vals),
+                        _ptr(ws), ws.numel() * ws.element_size() if ws is not None else 0,
                         _stream(stream))
 
 
@@ -220,12 +228,17 @@ def score_group(latent, lat_scale, q_abs, q_abs_scale, w, beta=None, q_pos=None,
     return out
 
 
-def topk(scores, k: int, valid_len=None, with_vals: bool = False, out=None, stream=None):
-    """Per-row TopK: returns idx [..., k] int32 (and vals when asked)."""
+def topk(scores, k: int, valid_len=None, with_vals: bool = False, out=None, ws=None, stream=None):
+    """Per-row TopK: returns idx [..., k] int32 (and vals when asked).  Long rows
+    get a workspace (allocated here unless `ws` is given) for the two-pass path."""
     shape = scores.shape[:-1] + (k,)
     idx = out if out is not None else torch.empty(shape, dtype=torch.int32, device=scores.device)
     vals = torch.empty(shape, dtype=torch.float32, device=scores.device) if with_vals else None
-    _check(li_topk(scores, k, idx, vals, valid_len, stream), "li_topk")
+    if ws is None and valid_len is None and scores.shape[-1] > 0:
+        n = li_topk_workspace_size(scores.numel() // scores.shape[-1], scores.shape[-1], k)
+        if n > 0:
+            ws = torch.empty(n, dtype=torch.uint8, device=scores.device)
+    _check(li_topk(scores, k, idx, vals, valid_len, ws, stream), "li_topk")
     return (idx, vals) if with_vals else idx
 
 

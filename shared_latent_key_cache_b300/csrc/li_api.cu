@@ -9,6 +9,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <climits>
 #include <cstdint>
 
 #include "li_internal.cuh"
@@ -42,6 +43,59 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 bool valid_dtype(int t) { return t == LI_F32 || t == LI_BF16 || t == LI_FP8_E4M3; }
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// Two-pass selection of long rows: pass 1 takes the exact top-k of every
+// kTopkRegRow-score segment (candidates carry their position in the whole
+// row; unused slots hold position INT32_MAX and -inf), pass 2 the top-k of a
+// row's segment candidates, ties broken through the candidates' positions.
+// The global top-k is inside the union of the segments' top-k (fewer than k
+// scores of the row beat any member, so fewer than k of its segment do), so
+// the result equals a one-pass selection.  Used for rows without a valid
+// length whose segment candidates fit one register-resident row.
+int64_t topk_segments(int L, int k)
+{
+    if (L <= kTopkRegRow || k <= 0 || k > kTopkRegRow)
+        return 0;
+    const int64_t S = (static_cast<int64_t>(L) + kTopkRegRow - 1) / kTopkRegRow;
+    return S * k <= kTopkRegRow ? S : 0;
+}
+
+size_t topk_two_pass_bytes(int64_t rows, int L, int k)
+{
+    const int64_t S = topk_segments(L, k);
+    if (rows <= 0 || S == 0)
+        return 0;
+    return 2 * align256(sizeof(float) * static_cast<size_t>(rows * S * k));
+}
+
+// p: the one-pass parameters (rows_per_group == 1, no map, no valid_len).
+cudaError_t launch_topk_two_pass(const TopkParams &p, void *ws, cudaStream_t s)
+{
+    const int64_t S = topk_segments(p.L_row, p.k);
+    const size_t n = static_cast<size_t>(p.rows * S * p.k);
+    float *cv = static_cast<float *>(ws);
+    int32_t *ci = reinterpret_cast<int32_t *>(static_cast<uint8_t *>(ws) + align256(sizeof(float) * n));
+    TopkParams a = p;
+    a.rows = p.rows * S;
+    a.idx = ci;
+    a.vals = cv;
+    a.rows_per_group = 1;
+    a.group_stride = 1;
+    a.row_offset = 0;
+    a.segs = static_cast<int>(S);
+    a.seg_len = kTopkRegRow;
+    a.pad_idx = INT32_MAX;
+    cudaError_t e = launch_topk(a, s);
+    if (e != cudaSuccess)
+        return e;
+    TopkParams b = p;
+    b.scores = cv;
+    b.in_stride = S * p.k;
+    b.L_row = static_cast<int>(S * p.k);
+    b.map = ci;
+    b.map_stride = S * p.k;
+    return launch_topk(b, s);
+}
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? LI_OK : LI_ERR_CUDA; }
 
@@ -194,14 +248,20 @@ int li_score_group(const void *latent, int lat_t, const float *lat_scale, const 
     return run_score(p, static_cast<cudaStream_t>(stream));
 }
 
+size_t li_topk_workspace_size(int64_t rows, int L, int k)
+{
+    return topk_two_pass_bytes(rows, L, k);
+}
+
 int li_topk(const float *scores, int64_t rows, int L, const int32_t *valid_len, int k, int32_t *idx,
-            float *vals, void *stream)
+            float *vals, void *ws, size_t ws_bytes, void *stream)
 {
     if (!scores || !idx)
         return LI_ERR_INVALID_ARG;
     if (rows < 0 || L < 0 || k <= 0 || k > (1 << 30))
         return LI_ERR_INVALID_ARG;
-    if (!aligned16(scores) || !aligned16(idx) || !aligned16(vals) || !aligned16(valid_len))
+    if (!aligned16(scores) || !aligned16(idx) || !aligned16(vals) || !aligned16(valid_len) ||
+        !aligned16(ws))
         return LI_ERR_ALIGNMENT;
     if (rows == 0)
         return LI_OK;
@@ -222,6 +282,9 @@ int li_topk(const float *scores, int64_t rows, int L, const int32_t *valid_len, 
     p.status = device_status_ptr();
     if (!p.status)
         return LI_ERR_CUDA;
+    const size_t two = topk_two_pass_bytes(rows, L, k);
+    if (ws && two > 0 && ws_bytes >= two && !valid_len)
+        return cuda_status(launch_topk_two_pass(p, ws, static_cast<cudaStream_t>(stream)));
     return cuda_status(launch_topk(p, static_cast<cudaStream_t>(stream)));
 }
 
@@ -232,7 +295,7 @@ size_t li_hs_workspace_size(int B, int G, int L, int m, int k)
     const size_t anchor = align256(sizeof(float) * static_cast<size_t>(B) * L);
     const size_t cvals = align256(sizeof(float) * static_cast<size_t>(B) * m);
     const size_t fol = align256(sizeof(float) * static_cast<size_t>(B) * (G - 1) * m);
-    return anchor + cvals + fol;
+    return anchor + cvals + fol + topk_two_pass_bytes(B, L, m);
 }
 
 int li_hs_select(const void *latent, int lat_t, const float *lat_scale, const void *q_abs, int abs_t,
@@ -259,6 +322,8 @@ int li_hs_select(const void *latent, int lat_t, const float *lat_scale, const vo
     float *cvals = reinterpret_cast<float *>(wsb + align256(sizeof(float) * static_cast<size_t>(B) * L));
     float *fol = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(cvals) +
                                            align256(sizeof(float) * static_cast<size_t>(B) * m));
+    void *tws = reinterpret_cast<uint8_t *>(fol) +
+                align256(sizeof(float) * static_cast<size_t>(B) * (G - 1) * m);   // anchor top-m passes
     const int nc = m < L ? m : L;
 
     ScoreParams a{};
@@ -319,7 +384,8 @@ int li_hs_select(const void *latent, int lat_t, const float *lat_scale, const vo
     t.map = nullptr;
     t.map_stride = 0;
     t.status = status;
-    st = cuda_status(launch_topk(t, s));
+    st = cuda_status(topk_two_pass_bytes(B, L, m) > 0 ? launch_topk_two_pass(t, tws, s)
+                                                      : launch_topk(t, s));
     if (st != LI_OK)
         return st;
     // 3. the anchor's own top-k, inside its candidates

@@ -84,8 +84,17 @@ struct TopkParams {
     const int32_t *map;
     int64_t map_stride;
     int *status;
+    // segmented rows (first pass of the two-pass long-row selection): row i is
+    // positions [s * seg_len, (s + 1) * seg_len) of score row i / segs,
+    // s = i % segs; outputs are positions in the whole row.  Needs map and
+    // valid_len NULL.
+    int segs = 1;
+    int seg_len = 0;
+    int pad_idx = -1;   // index written to output slots past min(k, V)
 };
 cudaError_t launch_topk(const TopkParams &p, cudaStream_t s);
+// Longest row (and segment) the register-resident top-k takes.
+constexpr int kTopkRegRow = 32768;
 
 // Launches `kern` on stream `s` with programmatic stream serialization: the
 // kernel may be scheduled while its predecessor in the stream finishes.  The

@@ -695,11 +695,22 @@ __global__ void __launch_bounds__(kThreads, 1) topk_reg_kernel(const TopkParams 
     griddep_launch_dependents();
 
     for (int64_t row = blockIdx.x; row < p.rows; row += gridDim.x) {
-        const float *src = p.scores + row * p.in_stride;
-        int V = p.L_row;
+        // A segmented row (p.segs > 1) is score row row / segs, positions
+        // [s * seg_len, s * seg_len + Lr) with s = row % segs; its outputs are
+        // positions in the whole row (pos_off added), valid_len is not used.
+        int64_t rrow = row;
+        int pos_off = 0;
+        int Lr = p.L_row;
+        if (p.segs > 1) {
+            rrow = row / p.segs;
+            pos_off = static_cast<int>(row % p.segs) * p.seg_len;
+            Lr = min(p.seg_len, p.L_row - pos_off);
+        }
+        const float *src = p.scores + rrow * p.in_stride + pos_off;
+        int V = Lr;
         if (p.valid_len != nullptr) {
             V = p.valid_len[row];
-            V = V < 0 ? 0 : (V > p.L_row ? p.L_row : V);
+            V = V < 0 ? 0 : (V > Lr ? Lr : V);
         }
         const int64_t grp = row / p.rows_per_group;
         const int64_t orow = grp * p.group_stride + row % p.rows_per_group + p.row_offset;
@@ -707,15 +718,17 @@ __global__ void __launch_bounds__(kThreads, 1) topk_reg_kernel(const TopkParams 
         float *oval = p.vals ? p.vals + orow * p.k : nullptr;
         const int32_t *map = p.map ? p.map + grp * p.map_stride : nullptr;
         const int nsel = p.k < V ? p.k : V;
+        // output index of row position pos (map and pos_off are never both used)
+        auto gpos = [&](int pos) -> int { return map ? map[pos] : pos + pos_off; };
 
         for (int j = nsel + tid; j < p.k; j += kThreads) {      // padding
-            oidx[j] = -1;
+            oidx[j] = p.pad_idx;
             if (oval)
                 oval[j] = -__int_as_float(0x7f800000);
         }
         if (nsel == V) {
             for (int j = tid; j < V; j += kThreads) {
-                oidx[j] = map ? map[j] : j;
+                oidx[j] = gpos(j);
                 if (oval)
                     oval[j] = src[j];
             }
@@ -726,16 +739,16 @@ __global__ void __launch_bounds__(kThreads, 1) topk_reg_kernel(const TopkParams 
         // ---- load: element e of this thread is at position 4 (tid + 1024 (e / 4)) + e % 4
         uint32_t key[kRegPer];
         const bool al16 = (reinterpret_cast<uintptr_t>(src) & 15u) == 0;
-        if (al16 && (p.L_row & 3) == 0) {
+        if (al16 && (Lr & 3) == 0) {
             // All eight 16-byte loads of the thread in flight at once: a load is
-            // skipped only past the row's storage (p.L_row), positions in
-            // [V, p.L_row) are read and then ignored through valid().
+            // skipped only past the row's storage (Lr), positions in
+            // [V, Lr) are read and then ignored through valid().
             const float4 *r4 = reinterpret_cast<const float4 *>(src);
             float4 v[kRegPer / 4];
 #pragma unroll
             for (int i = 0; i < kRegPer / 4; ++i) {
                 const int q = tid + kThreads * i;
-                v[i] = 4 * q < p.L_row ? __ldg(r4 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+                v[i] = 4 * q < Lr ? __ldg(r4 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
 #pragma unroll
             for (int i = 0; i < kRegPer / 4; ++i) {
@@ -839,11 +852,11 @@ __global__ void __launch_bounds__(kThreads, 1) topk_reg_kernel(const TopkParams 
                     if (valid(e) && o >= lo_off) {
                         const int pos = 4 * (tid + kThreads * (e >> 2)) + (e & 3);
                         if (o > hi_off) {
-                            oidx[so] = pos;
+                            oidx[so] = pos + pos_off;
                             ++so;
                         } else {
                             sm.ckey[co] = key[e];
-                            sm.cpos[co] = pos;
+                            sm.cpos[co] = pos + pos_off;
                             ++co;
                         }
                     }
@@ -855,13 +868,13 @@ __global__ void __launch_bounds__(kThreads, 1) topk_reg_kernel(const TopkParams 
                     if (valid(e) && o >= lo_off) {
                         const int pos = 4 * (tid + kThreads * (e >> 2)) + (e & 3);
                         if (o > hi_off) {
-                            oidx[so] = map ? map[pos] : pos;
+                            oidx[so] = gpos(pos);
                             if (oval)
                                 oval[so] = key_float(key[e]);
                             ++so;
                         } else {
                             sm.ckey[co] = key[e];
-                            sm.cpos[co] = map ? map[pos] : pos;
+                            sm.cpos[co] = gpos(pos);
                             ++co;
                         }
                     }
@@ -1030,7 +1043,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_reg_kernel(const TopkParams 
         for (int e = 0; e < kRegPer; ++e) {
             if (valid(e) && key[e] > K) {
                 const int pos = 4 * (tid + kThreads * (e >> 2)) + (e & 3);
-                oidx[slot] = map ? map[pos] : pos;
+                oidx[slot] = gpos(pos);
                 if (oval)
                     oval[slot] = key_float(key[e]);
                 ++slot;
@@ -1043,7 +1056,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_reg_kernel(const TopkParams 
                 if (valid(e) && key[e] == K) {
                     const int pos = 4 * (tid + kThreads * (e >> 2)) + (e & 3);
                     const int s2 = static_cast<int>(sure) + atomicAdd(&sm.slot, 1);
-                    oidx[s2] = map ? map[pos] : pos;
+                    oidx[s2] = gpos(pos);
                     if (oval)
                         oval[s2] = key_float(K);
                 }
@@ -1107,7 +1120,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_reg_kernel(const TopkParams 
                     if (valid(e) && key[e] == K) {
                         if (r < need) {
                             const int pos = 4 * (tid + kThreads * i) + j;
-                            oidx[sure + r] = map ? map[pos] : pos;
+                            oidx[sure + r] = gpos(pos);
                             if (oval)
                                 oval[sure + r] = key_float(K);
                         }
@@ -1143,7 +1156,8 @@ cudaError_t launch_topk(const TopkParams &p, cudaStream_t s)
         attr_set[dev].store(1, std::memory_order_relaxed);
     }
     const int64_t grid = p.rows < 0x7FFFFFFF ? p.rows : 0x7FFFFFFF;
-    if (p.L_row <= kRegRow)
+    static_assert(kRegRow == kTopkRegRow, "register-resident row length");
+    if (p.segs > 1 || p.L_row <= kRegRow)
         return launch_pdl(topk_reg_kernel, dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, s, p);
     return launch_pdl(topk_kernel, dim3(static_cast<unsigned>(grid)), dim3(kThreads), static_cast<size_t>(smem), s, p);
 }

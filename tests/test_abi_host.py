@@ -99,17 +99,32 @@ def test_absorb_argument_errors(L):
 def test_topk_argument_errors(L):
     f = L.li_topk
     f.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
-                  ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
-    assert f(None, 4, 100, None, 10, A, None, None) == LI_ERR_INVALID_ARG
-    assert f(A, 4, 100, None, 0, A, None, None) == LI_ERR_INVALID_ARG
-    assert f(A, -1, 100, None, 10, A, None, None) == LI_ERR_INVALID_ARG
-    assert f(MIS, 4, 100, None, 10, A, None, None) == LI_ERR_ALIGNMENT
-    assert f(A, 0, 100, None, 10, A, None, None) == LI_OK        # nothing to do, no CUDA call
+                  ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+    assert f(None, 4, 100, None, 10, A, None, None, 0, None) == LI_ERR_INVALID_ARG
+    assert f(A, 4, 100, None, 0, A, None, None, 0, None) == LI_ERR_INVALID_ARG
+    assert f(A, -1, 100, None, 10, A, None, None, 0, None) == LI_ERR_INVALID_ARG
+    assert f(MIS, 4, 100, None, 10, A, None, None, 0, None) == LI_ERR_ALIGNMENT
+    assert f(A, 4, 100, None, 10, A, None, MIS, 1 << 20, None) == LI_ERR_ALIGNMENT
+    assert f(A, 0, 100, None, 10, A, None, None, 0, None) == LI_OK   # nothing to do, no CUDA call
+
+
+def test_topk_workspace_size(L):
+    f = L.li_topk_workspace_size
+    f.argtypes = [ctypes.c_int64, ctypes.c_int, ctypes.c_int]
+    f.restype = ctypes.c_size_t
+    # rows of 131,072 in four 32,768-score segments: candidates (value + index) per row and segment
+    assert f(32, 131072, 2048) == 2 * 32 * 4 * 2048 * 4
+    assert f(8, 131072, 8192) == 2 * 8 * 4 * 8192 * 4
+    assert f(3, 40000, 100) == 2 * 2560                # 3 rows x 2 segments x 100 x 4 B, 256-aligned
+    assert f(32, 32768, 2048) == 0                     # one segment: one pass
+    assert f(4, 131072, 16384) == 0                    # candidates exceed one register-resident row
+    assert f(0, 131072, 2048) == 0
 
 
 def test_hs_workspace_size_and_errors(L):
     ws = L.li_hs_workspace_size(8, 4, 131072, 8192, 2048)
-    assert ws == 8 * 131072 * 4 + 8 * 8192 * 4 + 8 * 3 * 8192 * 4
+    # anchor scores, candidate scores, follower scores, anchor top-m in two passes
+    assert ws == 8 * 131072 * 4 + 8 * 8192 * 4 + 8 * 3 * 8192 * 4 + 2 * 8 * 4 * 8192 * 4
     assert L.li_hs_workspace_size(0, 4, 10, 10, 10) == 0
     f = L.li_hs_select
     args = [A, FP8, A, A, FP8, A, A, None, 2, 4, 64, 192, 1000, 256, 64, A, A, A, ws, None]

@@ -193,6 +193,33 @@ def test_topk_short_threshold_list_with_ties(li, orc):
         np.testing.assert_array_equal(np.sort(gv, axis=1), np.sort(ov.astype(np.float32), axis=1))
 
 
+def test_topk_two_pass_equals_one_pass(li, orc):
+    """Rows longer than 32,768 with a workspace take the two-pass path (segment
+    top-k, then top-k of the candidates): same sets and values as one pass and
+    as the oracle, including ties that straddle segments."""
+    g = torch.Generator().manual_seed(22)
+    s = torch.randn(5, 131072, generator=g) * 4 + 10
+    s[1] = torch.randint(0, 9, (131072,), generator=g).float()     # ties across segments
+    s[2, 40000:100000] = s[2].max() + 1.0                           # one value over two segments
+    s[3, ::3] = float("-inf")
+    sd = s.to(DEV)
+    for k in (1, 100, 2048, 8192):
+        n = li.li_topk_workspace_size(5, 131072, k)
+        assert n > 0
+        ws = torch.empty(n, dtype=torch.uint8, device=DEV)
+        i1 = torch.empty(5, k, dtype=torch.int32, device=DEV)
+        v1 = torch.empty(5, k, dtype=torch.float32, device=DEV)
+        i2 = torch.empty_like(i1)
+        v2 = torch.empty_like(v1)
+        assert li.li_topk(sd, k, i1, v1, ws=ws) == 0
+        assert li.li_topk(sd, k, i2, v2) == 0
+        _sync_ok(li)
+        oi, ov = orc.topk(s.double().numpy(), k)
+        exact_sets_equal(i1.cpu().numpy(), oi)
+        exact_sets_equal(i2.cpu().numpy(), oi)
+        np.testing.assert_array_equal(np.sort(v1.cpu().numpy(), axis=1), np.sort(v2.cpu().numpy(), axis=1))
+
+
 def test_topk_threshold_bin_overflows_shared_memory(li, orc):
     """Scores sharing their top 12 key bits (one exponent, same 3 mantissa bits) force the
     re-read path; a narrower cluster forces the second-digit re-read too."""
@@ -359,6 +386,17 @@ def test_hs_many_ties_at_the_follower_threshold(li, orc):
     lat, sc = x["latent"].clone(), x["lat_scale"].clone()
     lat[:, 3000:] = 0
     _hs_exact_vs_scan(li, orc, lat, sc, x, 8192, 5000)
+
+
+def test_hs_long_anchor_row_two_pass_with_ties(li, orc):
+    """An anchor row longer than 32,768 takes its top-m in two passes from the
+    HS workspace; duplicated latent rows make ties straddle the segments."""
+    w = li_inputs.spec("fp8_128k_hs", B=1, L=40000, m=8192, k=2048)
+    x = li_inputs.make_workload(w, seed=10)
+    lat, sc = x["latent"].clone(), x["lat_scale"].clone()
+    lat[:, 20000:] = lat[:, :20000]
+    sc[:, 20000:] = sc[:, :20000]
+    _hs_exact_vs_scan(li, orc, lat, sc, x, 8192, 2048)
 
 
 @pytest.mark.parametrize("d,r", [(40, 64), (36, 100), (128, 256)])
