@@ -8,12 +8,12 @@
 // contraction  [query rows x d] x [d x r]:  one CTA takes a tile of 128 query
 // rows (128/H queries x H heads, loaded by TMA as a 4D box) and the layer's
 // decoder, issues kind::f16 tcgen05 MMAs (M = 128 rows, N = r, fp32
-// accumulation in tensor memory), and its four warps read the result back one
-// row per thread.  Each thread therefore owns a whole output row, so the fp8
-// per-row scale (max|row| / 448) needs no cross-thread reduction: a first pass
-// over the row's TMEM columns finds the maximum, a second converts (E4M3,
-// round to nearest even, saturating) and stores.  bf16 and fp32 outputs are
-// stored in one pass.
+// accumulation in tensor memory), and eight warps read the result back: two
+// per TMEM lane quarter, each thread holding one output row's half (r/2
+// columns) in registers after a single round of loads.  The fp8 per-row scale
+// (max|row| / 448) combines the two halves' maxima through shared memory;
+// the thread then converts (E4M3, round to nearest even, saturating) and
+// stores its half.  bf16 and fp32 outputs are converted and stored directly.
 //
 // Operands are K-major bf16 in 64-element (128-byte) K chunks with the
 // 128-byte swizzle, as TMA writes them; both fit in shared memory at once
@@ -32,7 +32,7 @@
 namespace li {
 namespace {
 
-constexpr int kThreads = 128;       // 4 warps: TMEM lane quarters = 128 rows
+constexpr int kThreads = 256;       // 8 warps: two per TMEM lane quarter (128 rows)
 constexpr int kTileRows = 128;
 constexpr int kChunk = 64;          // bf16 elements per 128-byte K chunk
 constexpr int kMaxDev = 64;
@@ -47,6 +47,18 @@ struct AbsTcCfg {
     int tmem_cols;
 };
 
+// Ties the registers of a finished 16-column tcgen05.ld to the preceding
+// wait::ld (which covers every outstanding load of the thread).
+__device__ __forceinline__ void regs_ready16(uint32_t (&v)[16])
+{
+    asm volatile(""
+                 : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]), "+r"(v[6]),
+                   "+r"(v[7]), "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]), "+r"(v[12]), "+r"(v[13]),
+                   "+r"(v[14]), "+r"(v[15])
+                 :
+                 : "memory");
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     absorb_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmD,
                      const AbsorbParams p, const AbsTcCfg c, int *status)
@@ -54,6 +66,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint32_t tmem_base_s;
     __shared__ int abort_s;
+    __shared__ float amax_part[2][kTileRows];     // fp8: row maxima of the two column halves
     const uint32_t raw_u32 = smem_u32(smem_raw);
     uint8_t *base = smem_raw + (((raw_u32 + 1023u) & ~1023u) - raw_u32);
     uint8_t *smA = base;
@@ -119,83 +132,98 @@ __global__ void __launch_bounds__(kThreads, 1)
     ok = __all_sync(0xffffffffu, mbar_wait(bar_mma, 0, abort_flag, status, kWaitLimitNs)) &&
          *abort_flag == 0;
     tc_fence_after();
-    const int row = warp * 32 + lane;                 // TMEM lane = tile row
+    // Two warps per TMEM lane quarter (warp % 4): warp w reads its quarter's
+    // rows, columns [half * r/2, (half + 1) * r/2) with half = w / 4, all in
+    // one round of loads, so every value is read from TMEM once.
+    const int quarter = warp & 3;
+    const int half = warp >> 2;
+    const int hc = p.r / 2;                           // columns per thread (16 ... 128)
+    const int n16 = hc / 16;
+    const int row = quarter * 32 + lane;              // TMEM lane = tile row
     const int qi = row / p.H;
     const int h = row % p.H;
     const int64_t n = static_cast<int64_t>(tile) * c.qpt + qi;
     const bool live = ok && n < p.N;
     const int64_t orow = (n * p.G + l) * p.H + h;      // output row index
-    const uint32_t trow = tmem_base + (static_cast<uint32_t>(warp * 32) << 16);
+    const uint32_t tcol = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                          static_cast<uint32_t>(half * hc);
+    uint32_t v[8][16];
     if (ok) {
-        if (p.abs_t == LI_FP8_E4M3) {
-            float amax = 0.f;
-            for (int c0 = 0; c0 < p.r; c0 += 32) {
-                uint32_t v[32];
-                tmem_ld32(trow + static_cast<uint32_t>(c0), v);
-                tmem_ld_wait32(v);
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    amax = fmaxf(amax, fabsf(__uint_as_float(v[j])));
-            }
-            const float inv = amax > 0.f ? 448.f / amax : 0.f;
-            uint8_t *out = static_cast<uint8_t *>(p.q_abs) + orow * p.r;
-            for (int c0 = 0; c0 < p.r; c0 += 32) {
-                uint32_t v[32];
-                tmem_ld32(trow + static_cast<uint32_t>(c0), v);
-                tmem_ld_wait32(v);
+        for (int j = 0; j < 8; ++j)
+            if (j < n16)
+                tmem_ld16(tcol + static_cast<uint32_t>(16 * j), v[j]);
+        tmem_ld_wait16(v[0]);
+#pragma unroll
+        for (int j = 1; j < 8; ++j)
+            regs_ready16(v[j]);
+    }
+    if (p.abs_t == LI_FP8_E4M3) {
+        // the row maximum: this thread's half, then the partner warp's
+        float amax = 0.f;
+        if (ok) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (j < n16) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        amax = fmaxf(amax, fabsf(__uint_as_float(v[j][i])));
+                }
+        }
+        amax_part[half][row] = amax;
+        __syncthreads();
+        amax = fmaxf(amax_part[0][row], amax_part[1][row]);
+        const float inv = amax > 0.f ? 448.f / amax : 0.f;
+        if (ok) {
+            uint8_t *out = static_cast<uint8_t *>(p.q_abs) + orow * p.r + half * hc;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (j < n16) {
+                    uint32_t packed[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
+                            make_float2(__uint_as_float(v[j][4 * i]) * inv, __uint_as_float(v[j][4 * i + 1]) * inv),
+                            __NV_SATFINITE, __NV_E4M3);
+                        const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
+                            make_float2(__uint_as_float(v[j][4 * i + 2]) * inv, __uint_as_float(v[j][4 * i + 3]) * inv),
+                            __NV_SATFINITE, __NV_E4M3);
+                        packed[i] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+                    }
+                    if (live)
+                        reinterpret_cast<uint4 *>(out)[j] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                }
+            if (live && half == 0)
+                p.q_abs_scale[orow] = amax / 448.f;
+        }
+    } else if (ok && p.abs_t == LI_BF16) {
+        __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.q_abs) + orow * p.r + half * hc;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (j < n16) {
                 uint32_t packed[8];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
-                        make_float2(__uint_as_float(v[4 * j]) * inv, __uint_as_float(v[4 * j + 1]) * inv),
-                        __NV_SATFINITE, __NV_E4M3);
-                    const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
-                        make_float2(__uint_as_float(v[4 * j + 2]) * inv, __uint_as_float(v[4 * j + 3]) * inv),
-                        __NV_SATFINITE, __NV_E4M3);
-                    packed[j] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+                for (int i = 0; i < 8; ++i) {
+                    const __nv_bfloat162 b2 =
+                        __floats2bfloat162_rn(__uint_as_float(v[j][2 * i]), __uint_as_float(v[j][2 * i + 1]));
+                    packed[i] = *reinterpret_cast<const uint32_t *>(&b2);
                 }
                 if (live) {
-                    uint4 *o4 = reinterpret_cast<uint4 *>(out + c0);
+                    uint4 *o4 = reinterpret_cast<uint4 *>(out + 16 * j);
                     o4[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
                     o4[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
                 }
             }
-            if (live)
-                p.q_abs_scale[orow] = amax / 448.f;
-        } else if (p.abs_t == LI_BF16) {
-            __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.q_abs) + orow * p.r;
-            for (int c0 = 0; c0 < p.r; c0 += 32) {
-                uint32_t v[32];
-                tmem_ld32(trow + static_cast<uint32_t>(c0), v);
-                tmem_ld_wait32(v);
-                uint32_t packed[16];
+    } else if (ok) {
+        float *out = static_cast<float *>(p.q_abs) + orow * p.r + half * hc;
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const __nv_bfloat162 b2 =
-                        __floats2bfloat162_rn(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
-                    packed[j] = *reinterpret_cast<const uint32_t *>(&b2);
-                }
-                if (live) {
-                    uint4 *o4 = reinterpret_cast<uint4 *>(out + c0);
+        for (int j = 0; j < 8; ++j)
+            if (j < n16 && live) {
+                uint4 *o4 = reinterpret_cast<uint4 *>(out + 16 * j);
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        o4[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
-                }
+                for (int i = 0; i < 4; ++i)
+                    o4[i] = make_uint4(v[j][4 * i], v[j][4 * i + 1], v[j][4 * i + 2], v[j][4 * i + 3]);
             }
-        } else {
-            float *out = static_cast<float *>(p.q_abs) + orow * p.r;
-            for (int c0 = 0; c0 < p.r; c0 += 32) {
-                uint32_t v[32];
-                tmem_ld32(trow + static_cast<uint32_t>(c0), v);
-                tmem_ld_wait32(v);
-                if (live) {
-                    uint4 *o4 = reinterpret_cast<uint4 *>(out + c0);
-#pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        o4[q] = make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-                }
-            }
-        }
     }
     tc_fence_before();
     __syncthreads();
@@ -218,7 +246,7 @@ bool make_cfg(const AbsorbParams &p, AbsTcCfg &c, int &smem)
         cols <<= 1;
     c.tmem_cols = cols;
     smem = c.off_bar + 16 + 1024;
-    return smem <= 227 * 1024 - 64;   // the kernel's static shared memory comes on top
+    return smem <= 227 * 1024 - 2048;   // the kernel's static shared memory comes on top
 }
 
 } // namespace
