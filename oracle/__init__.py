@@ -63,8 +63,9 @@ def lib():
         L.or_topk.argtypes = [P, I64, I, P, I, P, P, I]
         L.or_hs.argtypes = [P, I, I, I, I, I, P, P, I]
         L.or_native_score.argtypes = [P, I, P, P, P, I, I, I, I, P, I]
+        L.or_append_latent.argtypes = [P, I, P, I, I, I, I, I, ctypes.c_double, P, P, I]
         for f in ("or_decode_rows", "or_absorb", "or_reconstruct_keys", "or_score", "or_topk",
-                  "or_hs", "or_native_score"):
+                  "or_hs", "or_native_score", "or_append_latent"):
             getattr(L, f).restype = None
         _lib = L
     return _lib
@@ -206,6 +207,19 @@ def hs(scores, m: int, k: int, nthreads: int | None = None):
     idx = np.empty((B, G, k), dtype=np.int32)
     lib().or_hs(_p(sa), B, G, L, m, k, _p(cand), _p(idx), nthreads or default_threads())
     return cand, idx
+
+
+def append_latent(x, P, rR: int, pos, base: float = 10000.0, nthreads: int | None = None) -> np.ndarray:
+    """Eqs. (1)-(2): c = [Q_t P_R^T x ; P_N^T x] per sequence.  x [B][dm],
+    P [r][dm] (rows < rR: P_R^T), pos [B] -> c [B][r] fp64 (before storage)."""
+    xa, Pa = np.ascontiguousarray(_np(x)), np.ascontiguousarray(_np(P))
+    B, dm = xa.shape
+    r = Pa.shape[0]
+    pa = np.ascontiguousarray(_np(pos), dtype=np.int32).reshape(-1)
+    out = np.empty((B, r), dtype=np.float64)
+    lib().or_append_latent(_p(xa), _code(xa), _p(Pa), _code(Pa), B, dm, r, rR, float(base), _p(pa),
+                           _p(out), nthreads or default_threads())
+    return out
 
 
 def native_score(keys, key_scale, q, w, nthreads: int | None = None) -> np.ndarray:

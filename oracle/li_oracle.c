@@ -17,6 +17,9 @@
  *        (explainer page): native DSA indexer key cache of 132 B per token per
  *        layer (fp8 keys + scale), the 192-value latent, the absorption
  *        identity q.(D c) = (D^T q).c, and HS with an 8,192-token cart.
+ *   [S] Methodology, "Shared Latent Cache", eqs. (1)-(2): the latent of a
+ *        token is built from the anchor layer's hidden state x as
+ *        z^N = P_N^T x, z^R = Q_t P_R^T x, c = [z^R; z^N].
  *
  * Notation.  A decoder is stored as D_l with shape r x d (r = latent rank,
  * d = per-layer indexer key width), so the per-layer key of eq. (3) is
@@ -275,4 +278,35 @@ void or_native_score(const void *keys, int key_t, const float *key_scale, const 
                      const double *w, int B, int H, int d, int L, double *scores, int nthreads)
 {
     or_score(keys, key_t, key_scale, q, w, NULL, NULL, B, 1, 1, H, d, L, scores, nthreads);
+}
+
+/* Eqs. (1)-(2) of [S]: the shared latent of one new token per sequence.
+ *   x   [B][dm]  the anchor layer's hidden state of the token
+ *   P   [r][dm]  rows 0 .. rR-1 are P_R^T, rows rR .. r-1 are P_N^T
+ *   pos [B]      the token's position t
+ *   c   [B][r]   fp64 out: c = [Q_t P_R^T x ; P_N^T x]
+ * Q_t is the rotary position encoding: the RoPE branch is read as rR/2
+ * complex numbers (c_2i, c_2i+1), and number i is multiplied by
+ * exp(i t theta_i) with theta_i = base^(-2i/rR) ("complex linear combinations
+ * within each rotary frequency", [S] after eq. (4)). */
+void or_append_latent(const void *x, int x_t, const void *P, int P_t, int B, int dm, int r, int rR,
+                      double base, const int32_t *pos, double *c, int nthreads)
+{
+    #pragma omp parallel for num_threads(nthreads) schedule(static)
+    for (int b = 0; b < B; b++) {
+        double *cb = c + (int64_t)b * r;
+        for (int i = 0; i < r; i++) {
+            double acc = 0.0;
+            for (int j = 0; j < dm; j++)
+                acc += elem(P, P_t, (int64_t)i * dm + j) * elem(x, x_t, (int64_t)b * dm + j);
+            cb[i] = acc;
+        }
+        for (int i = 0; i < rR / 2; i++) {
+            const double theta = pow(base, -2.0 * i / rR);
+            const double ang = (double)pos[b] * theta;
+            const double re = cb[2 * i], im = cb[2 * i + 1];
+            cb[2 * i] = re * cos(ang) - im * sin(ang);
+            cb[2 * i + 1] = re * sin(ang) + im * cos(ang);
+        }
+    }
 }

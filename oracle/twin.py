@@ -87,3 +87,17 @@ def hs(scores: np.ndarray, m: int, k: int):
             sub = np.lexsort((C, -scores[b, l, C]))
             idx[b, l, :min(k, nc)] = C[sub[:min(k, nc)]]
     return cand, idx
+
+
+def append_latent(x: np.ndarray, P: np.ndarray, rR: int, pos, base: float = 10000.0) -> np.ndarray:
+    """Eqs. (1)-(2) of the summary page with complex arithmetic: the RoPE
+    branch of P x as rR/2 complex numbers, each multiplied by
+    exp(1j * t * base^(-2i/rR)).  x [B][dm], P [r][dm] (fp64 values) -> [B][r]."""
+    c = np.einsum("rd,bd->br", np.asarray(P, dtype=np.float64), np.asarray(x, dtype=np.float64))
+    t = np.asarray(pos, dtype=np.float64).reshape(-1, 1)
+    theta = base ** (-np.arange(0, rR, 2, dtype=np.float64) / rR)
+    z = (c[:, 0:rR:2] + 1j * c[:, 1:rR:2]) * np.exp(1j * t * theta)
+    out = c.copy()
+    out[:, 0:rR:2] = z.real
+    out[:, 1:rR:2] = z.imag
+    return out

@@ -375,3 +375,79 @@ def test_planted_wrong_tie_break_fails_brute_force():
     assert _brute_topk(row, 2) == [1, 2]
     wrong = sorted(range(4), key=lambda t: (-row[t], -t))[:2]
     assert wrong != _brute_topk(row, 2)
+
+
+# ------------------------------------------------- latent append, eqs. (1)-(2)
+
+def _append_case(B=3, dm=48, r=24, rR=8, seed=31):
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn(B, dm, generator=g, dtype=torch.float64)
+    P = torch.randn(r, dm, generator=g, dtype=torch.float64) / math.sqrt(dm)
+    return x.numpy(), P.numpy(), rR
+
+
+def test_append_at_position_zero_is_the_projection(orc):
+    x, P, rR = _append_case()
+    c = orc.append_latent(x, P, rR, np.zeros(3, dtype=np.int32))
+    np.testing.assert_allclose(c, x @ P.T, rtol=1e-12, atol=1e-12)
+
+
+def test_append_rotation_keeps_pair_norms_and_leaves_nope_alone(orc):
+    x, P, rR = _append_case()
+    pos = np.array([1, 777, 131071], dtype=np.int32)
+    c = orc.append_latent(x, P, rR, pos)
+    raw = x @ P.T
+    n_c = np.hypot(c[:, 0:rR:2], c[:, 1:rR:2])
+    n_raw = np.hypot(raw[:, 0:rR:2], raw[:, 1:rR:2])
+    np.testing.assert_allclose(n_c, n_raw, rtol=1e-12)
+    np.testing.assert_allclose(c[:, rR:], raw[:, rR:], rtol=1e-12, atol=1e-15)
+
+
+def test_append_rope_scores_depend_only_on_relative_position(orc):
+    """<Q_t a, Q_s b> = <Q_{t-s} a, b> on the RoPE branch: the property rotary
+    encoding is for (a wrong sign or frequency index breaks it)."""
+    x, P, rR = _append_case(B=2)
+    def rope_part(pos):
+        return orc.append_latent(x, P, rR, np.asarray(pos, dtype=np.int32))[:, :rR]
+    for t, s in ((5, 2), (1000, 37), (40000, 39999)):
+        a_t, b_s = rope_part([t, s])
+        a_d, b_0 = rope_part([t - s, 0])
+        lhs = float(a_t @ b_s)             # token 0 at t, token 1 at s
+        rhs = float(a_d @ b_0)             # token 0 at t - s, token 1 at 0
+        assert abs(lhs - rhs) <= 1e-9 * (abs(lhs) + 1.0)
+
+
+def test_append_frequency_schedule_on_unit_vectors(orc):
+    """A unit input on RoPE pair i comes out as (cos t.theta_i, sin t.theta_i),
+    theta_i = 10000^(-2i/rR): the first pair turns by t radians, the last
+    pair slowest."""
+    rR, r, dm = 8, 8, 8
+    P = np.eye(r, dm)
+    for i in range(rR // 2):
+        x = np.zeros((1, dm))
+        x[0, 2 * i] = 1.0
+        for t in (1, 3, 100):
+            c = orc.append_latent(x, P, rR, np.array([t], dtype=np.int32))[0]
+            ang = t * 10000.0 ** (-2.0 * i / rR)
+            np.testing.assert_allclose(c[2 * i:2 * i + 2], [math.cos(ang), math.sin(ang)], atol=1e-12)
+            assert np.abs(np.delete(c, [2 * i, 2 * i + 1])).max() < 1e-15
+
+
+def test_append_twin_matches_c_oracle(orc):
+    x, P, rR = _append_case(B=4, dm=64, r=40, rR=16, seed=32)
+    pos = np.array([0, 9, 4096, 131071], dtype=np.int32)
+    np.testing.assert_allclose(orc.append_latent(x, P, rR, pos), twin.append_latent(x, P, rR, pos),
+                               rtol=1e-11, atol=1e-12)
+
+
+def test_planted_reversed_rotation_fails_frequency_schedule():
+    """A rotation by -t.theta (a sign slip in Q_t) keeps norms and relative
+    positions but fails the unit-vector schedule."""
+    rR = dm = 4
+    P = np.eye(rR, dm)
+    x = np.zeros((1, dm))
+    x[0, 0] = 1.0
+    good = twin.append_latent(x, P, rR, [3])[0]
+    bad = twin.append_latent(x, P, rR, [-3])[0]          # same as rotating by -3 theta_0
+    np.testing.assert_allclose(good[:2], [math.cos(3.0), math.sin(3.0)], atol=1e-12)
+    assert abs(bad[1] - math.sin(3.0)) > 0.1
