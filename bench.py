@@ -498,6 +498,7 @@ def run_ours(a, w):
 
 def side_timings(a, w, x, q_abs, q_scale, li, stream, flush, dev):
     import torch
+    import li_inputs
     B, G, H, r, L, k, d = w.B, w.G, w.H, w.r, w.L, w.k, w.d
     out = {}
     reps = max(5, min(200, a.steps // 10))
@@ -516,6 +517,22 @@ def side_timings(a, w, x, q_abs, q_scale, li, stream, flush, dev):
             ts.append((e0, e1))
         torch.cuda.synchronize(dev)
         return statistics.median(e0.elapsed_time(e1) for e0, e1 in ts) * 1e3
+
+    # latent-cache append of one new token per sequence (eqs. 1-2): hidden size
+    # 7168 (DeepSeek-V3.2), RoPE branch 64 of the r latent values
+    dm, rR = 7168, 64 if r >= 64 else 0
+    xa, Pa = li_inputs.make_append_inputs(B, dm, r, "bf16", seed=a.seed, device=dev)
+    lat_dt = {"f32": torch.float32, "bf16": torch.bfloat16, "fp8": torch.uint8}[w.lat_dtype]
+    lat_a = torch.zeros(B, 8, r, dtype=lat_dt, device=dev)
+    sc_a = torch.zeros(B, 8, dtype=torch.float32, device=dev)
+    pos_a = torch.full((B,), 7, dtype=torch.int32, device=dev)
+
+    def append():
+        assert li.li_append_latent(xa, Pa, pos_a, rR, lat_a, sc_a, stream=stream) == 0
+    ap_us = timeit(append)
+    ap_bytes = r * dm * 2 + B * dm * 2 + B * (r * lat_a.element_size() + 4)
+    out["append"] = {"B": B, "d_model": dm, "r": r, "r_rope": rR, "latency_us": ap_us,
+                     "bytes": ap_bytes, "gbs": ap_bytes / (ap_us * 1e-6) / 1e9}
 
     m = w.m if w.m else 8192
     if m <= L:

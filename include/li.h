@@ -208,6 +208,32 @@ int li_native_score(const void *keys, int key_t, const float *key_scale,
                     int B, int H, int d, int L, float *scores, void *stream);
 
 /*
+ * Latent-cache append (summary page, Methodology, "Shared Latent Cache",
+ * eqs. (1)-(2)): for one new token per sequence, the shared latent
+ *     c = [Q_t P_R^T x ; P_N^T x]
+ * of the anchor layer's hidden state x, written into the cache at the
+ * token's position.  Q_t rotates the RoPE branch as complex pairs
+ * (c_2i, c_2i+1) by the angle t * rope_base^(-2i/rR).
+ *
+ *   x         [B][dm]  x_t in {LI_F32, LI_BF16}
+ *   P         [r][dm]  P_t in {LI_F32, LI_BF16}; rows 0 .. rR-1 are P_R^T,
+ *                      rows rR .. r-1 are P_N^T
+ *   pos       [B] int32: position t of the token (rotation angle) and the
+ *                      cache row it is written to
+ *   latent    [B][L][r] lat_t in {LI_F32, LI_BF16, LI_FP8_E4M3}: row pos[b]
+ *                      of sequence b is written, nothing else
+ *   lat_scale [B][L] fp32: required for LI_FP8_E4M3 (the row's scale
+ *                      max|c| / 448 is written at pos[b]), ignored otherwise
+ * fp32 accumulation; fp8 codes rounded to nearest even, saturating.
+ * A position outside [0, L) writes nothing and latches LI_ERR_DEVICE_BOUNDS.
+ * Limits: 1 <= r <= 256, 0 <= rR <= r with rR even, 1 <= dm <= 2^24,
+ * rope_base > 0.
+ */
+int li_append_latent(const void *x, int x_t, const void *P, int P_t, const int32_t *pos,
+                     int B, int dm, int r, int rR, float rope_base,
+                     void *latent, int lat_t, float *lat_scale, int L, void *stream);
+
+/*
  * Test hook for the device-side watchdog (no counterpart on the pages).
  * Launches one CTA that allocates tensor memory and waits, with the bounded
  * mbarrier wait every kernel of this library uses, on a barrier that nothing

@@ -166,6 +166,16 @@ def make_beta(B: int, T: int, G: int, H: int, seed: int = 0, device="cpu", std: 
     return (torch.randn(B, T, G, H, generator=g, device=device) * std).contiguous()
 
 
+def make_append_inputs(B: int, dm: int, r: int, dtype: str = "bf16", seed: int = 0, device="cpu"):
+    """Inputs of the latent append: the anchor layer's hidden states x [B][dm]
+    ~ N(0, 1) and the stacked projections P [r][dm] ~ N(0, 1/dm) (rows < rR
+    are P_R^T), stored as `dtype` ("f32" or "bf16")."""
+    x = torch.randn(B, dm, generator=_gen(seed, 21, "cpu"))
+    P = torch.randn(r, dm, generator=_gen(seed, 22, "cpu")) / dm ** 0.5
+    dt = {"f32": torch.float32, "bf16": torch.bfloat16}[dtype]
+    return x.to(dt).to(device), P.to(dt).to(device)
+
+
 def make_workload(w: Workload | str, seed: int = 0, device="cpu") -> dict:
     """All inputs of one workload as a dict of tensors on `device` (see module doc)."""
     if isinstance(w, str):

@@ -24,7 +24,7 @@ __all__ = [
     "li_version", "li_status_string", "li_absorb_queries", "li_score_group", "li_topk",
     "li_topk_workspace_size",
     "li_hs_workspace_size", "li_hs_select", "li_hs_select_noalloc", "li_native_score",
-    "li_device_status", "li_selftest_wait_timeout",
+    "li_device_status", "li_selftest_wait_timeout", "li_append_latent", "append_latent",
     "absorb_queries", "score_group", "topk", "hs_select", "native_score", "device_status",
 ]
 
@@ -63,9 +63,10 @@ def _load():
     L.li_hs_select_noalloc.argtypes = [P, I, P, P, I, P, P, P, I, I, I, I, I, I, I, P, P, P]
     L.li_device_status.argtypes = [P]
     L.li_selftest_wait_timeout.argtypes = [ctypes.c_uint, P]
+    L.li_append_latent.argtypes = [P, I, P, I, P, I, I, I, I, ctypes.c_float, P, I, P, I, P]
     for f in ("li_absorb_queries", "li_score_group", "li_topk", "li_hs_select",
               "li_native_score", "li_device_status", "li_hs_select_noalloc",
-              "li_selftest_wait_timeout"):
+              "li_selftest_wait_timeout", "li_append_latent"):
         getattr(L, f).restype = I
     return L
 
@@ -198,6 +199,17 @@ def li_device_status(stream=None) -> int:
     return _lib.li_device_status(_stream(stream))
 
 
+def li_append_latent(x, P, pos, rR: int, latent, lat_scale=None, rope_base: float = 10000.0,
+                     stream=None) -> int:
+    """x [B][dm], P [r][dm] (rows < rR: P_R^T), pos [B] int32 -> row pos[b] of latent [B][L][r]."""
+    B, dm = x.shape
+    r = P.shape[0]
+    L = latent.shape[1]
+    return _lib.li_append_latent(_ptr(x), _dtype_code(x), _ptr(P), _dtype_code(P), _ptr(pos), B, dm, r,
+                                 rR, float(rope_base), _ptr(latent), _dtype_code(latent),
+                                 _ptr(lat_scale), L, _stream(stream))
+
+
 def li_selftest_wait_timeout(limit_us: int, stream=None) -> int:
     """Launch the watchdog test kernel (a bounded wait that is never satisfied)."""
     return _lib.li_selftest_wait_timeout(int(limit_us), _stream(stream))
@@ -263,6 +275,12 @@ def native_score(keys, key_scale, q, q_scale, w, out=None, stream=None):
         out = torch.empty(B, L, dtype=torch.float32, device=keys.device)
     _check(li_native_score(keys, key_scale, q, q_scale, w, out, stream), "li_native_score")
     return out
+
+
+def append_latent(x, P, pos, rR: int, latent, lat_scale=None, rope_base: float = 10000.0,
+                  stream=None):
+    """Eqs. (1)-(2): writes the new tokens' latents into the cache (in place)."""
+    _check(li_append_latent(x, P, pos, rR, latent, lat_scale, rope_base, stream), "li_append_latent")
 
 
 def device_status(stream=None) -> int:

@@ -424,6 +424,44 @@ int li_native_score(const void *keys, int key_t, const float *key_scale, const v
                           d, L, scores, stream);
 }
 
+int li_append_latent(const void *x, int x_t, const void *P, int P_t, const int32_t *pos, int B,
+                     int dm, int r, int rR, float rope_base, void *latent, int lat_t, float *lat_scale,
+                     int L, void *stream)
+{
+    if (!x || !P || !pos || !latent || B < 0 || dm < 1 || dm > (1 << 24) || r < 1 || r > 256 ||
+        rR < 0 || rR > r || (rR & 1) || L < 1 || !(rope_base > 0.f))
+        return LI_ERR_INVALID_ARG;
+    if ((x_t != LI_F32 && x_t != LI_BF16) || (P_t != LI_F32 && P_t != LI_BF16) ||
+        (lat_t != LI_F32 && lat_t != LI_BF16 && lat_t != LI_FP8_E4M3))
+        return LI_ERR_INVALID_ARG;
+    if (lat_t == LI_FP8_E4M3 && !lat_scale)
+        return LI_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(P) || !aligned16(pos) || !aligned16(latent) || !aligned16(lat_scale))
+        return LI_ERR_ALIGNMENT;
+    if (B == 0)
+        return LI_OK;
+    AppendParams a{};
+    a.x = x;
+    a.P = P;
+    a.pos = pos;
+    a.latent = latent;
+    a.lat_scale = lat_scale;
+    a.x_t = x_t;
+    a.P_t = P_t;
+    a.lat_t = lat_t;
+    a.B = B;
+    a.dm = dm;
+    a.r = r;
+    a.rR = rR;
+    a.L = L;
+    a.base = rope_base;
+    a.vec = dm % 8 == 0;
+    a.status = device_status_ptr();
+    if (!a.status)
+        return LI_ERR_CUDA;
+    return cuda_status(launch_append(a, static_cast<cudaStream_t>(stream)));
+}
+
 int li_device_status(void *stream)
 {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)

@@ -40,6 +40,21 @@ cudaError_t launch_absorb(const AbsorbParams &p, cudaStream_t s);
 bool absorb_tc_supported(const AbsorbParams &p);
 cudaError_t launch_absorb_tc(const AbsorbParams &p, cudaStream_t s);
 
+// ------------------------------------------------------------- latent append
+struct AppendParams {
+    const void *x;         // [B][dm] anchor hidden state of the new token
+    const void *P;         // [r][dm]: rows < rR are P_R^T, the rest P_N^T
+    const int32_t *pos;    // [B] token position (rotary angle and cache row)
+    void *latent;          // [B][L][r]
+    float *lat_scale;      // [B][L] (fp8 caches)
+    int *status;
+    int x_t, P_t, lat_t;
+    int B, dm, r, rR, L;
+    float base;            // rotary base
+    bool vec;              // dm % 8 == 0 and 16-byte aligned rows: vector loads
+};
+cudaError_t launch_append(const AppendParams &p, cudaStream_t s);
+
 // ------------------------------------------------------------- scoring
 // One scoring launch evaluates eq. (8) for a contiguous range of Gs layers
 // [g0, g0 + Gs) of a group of Gtot layers, either over every cached token

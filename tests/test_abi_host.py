@@ -143,3 +143,29 @@ def test_native_argument_errors(L):
     assert f(None, FP8, A, A, FP8, A, A, 1, 64, 128, 100, A, None) == LI_ERR_INVALID_ARG
     assert f(A, FP8, None, A, FP8, A, A, 1, 64, 128, 100, A, None) == LI_ERR_INVALID_ARG
     assert f(A, FP8, A, A, FP8, A, A, 1, 64, 128, 0, A, None) == LI_ERR_INVALID_ARG
+
+
+def test_append_argument_errors(L):
+    f = L.li_append_latent
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
+                  ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float,
+                  ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]
+    ok = [A, BF16, A, BF16, A, 4, 7168, 192, 64, 10000.0, A, FP8, A, 1024, None]
+
+    def call(**kw):
+        args = list(ok)
+        names = ["x", "x_t", "P", "P_t", "pos", "B", "dm", "r", "rR", "base", "lat", "lat_t", "sc", "L", "s"]
+        for k, v in kw.items():
+            args[names.index(k)] = v
+        return f(*args)
+
+    assert call(x=None) == LI_ERR_INVALID_ARG
+    assert call(pos=None) == LI_ERR_INVALID_ARG
+    assert call(rR=63) == LI_ERR_INVALID_ARG          # RoPE pairs
+    assert call(rR=194) == LI_ERR_INVALID_ARG         # rR > r
+    assert call(r=300, rR=64) == LI_ERR_INVALID_ARG
+    assert call(sc=None) == LI_ERR_INVALID_ARG        # fp8 cache needs its scales
+    assert call(base=0.0) == LI_ERR_INVALID_ARG
+    assert call(lat_t=7) == LI_ERR_INVALID_ARG
+    assert call(x=MIS) == LI_ERR_ALIGNMENT
+    assert call(B=0) == LI_OK                         # nothing to do, no CUDA call
