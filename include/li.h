@@ -97,8 +97,10 @@ int li_absorb_queries(const void *q, int q_t, const void *D, int D_t,
  *                             query's causal limit are not written.
  * Supported dtype pairs: (F32, F32) on CUDA cores; (BF16, BF16) and
  * (FP8_E4M3, FP8_E4M3) on the tensor cores (tcgen05) when r % 64 == 0,
- * r <= 256, H in {16, 32, 64, 128} and G*H <= 256; any other pair or shape
- * runs on CUDA cores when G*H*r <= 8192 and r <= 256, else LI_ERR_UNSUPPORTED.
+ * r <= 256 and H in {16, 32, 64, 128}: in one pass over the cache when
+ * G*H <= 256, else in chunks of 256/H layers, one pass per chunk (G = 8 at
+ * H = 64: two passes); any other pair or shape runs on CUDA cores when
+ * G*H*r <= 8192 and r <= 256, else LI_ERR_UNSUPPORTED.
  */
 int li_score_group(const void *latent, int lat_t, const float *lat_scale,
                    const void *q_abs, int abs_t, const float *q_abs_scale,

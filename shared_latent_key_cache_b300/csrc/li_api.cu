@@ -130,10 +130,37 @@ int check_score_args(const void *latent, int lat_t, const float *lat_scale, cons
     return LI_OK;
 }
 
+// More layers than one tensor-core tile holds (Gs * H > 256): the layers are
+// scored in chunks of 256 / H, one pass over the cache per chunk, each chunk
+// writing its own rows of the score tensor.  Returns the layers per chunk, or
+// 0 when the chunks are not tensor-core shapes.
+int tc_chunk_layers(const ScoreParams &p)
+{
+    if (p.Gs <= 1 || p.H <= 0 || p.H > 256)
+        return 0;
+    ScoreParams q = p;
+    q.Gs = 256 / p.H;
+    return q.Gs >= 1 && q.Gs < p.Gs && score_tc_supported(q) ? q.Gs : 0;
+}
+
 int run_score(const ScoreParams &p, cudaStream_t s)
 {
     if (score_tc_supported(p))
         return cuda_status(launch_score_tc(p, s));
+    if (const int gc = tc_chunk_layers(p)) {
+        for (int c = 0; c < p.Gs; c += gc) {
+            ScoreParams q = p;
+            q.Gout = p.Gout ? p.Gout : p.Gs;
+            q.gout0 = p.gout0 + c;
+            q.g0 = p.g0 + c;
+            q.Gs = p.Gs - c < gc ? p.Gs - c : gc;
+            const int st = cuda_status(score_tc_supported(q) ? launch_score_tc(q, s)
+                                                             : launch_score_simt(q, s));
+            if (st != LI_OK)
+                return st;
+        }
+        return LI_OK;
+    }
     if (simt_smem(p.Gs, p.H, p.r) <= 227 * 1024)
         return cuda_status(launch_score_simt(p, s));
     return LI_ERR_UNSUPPORTED;
@@ -141,7 +168,7 @@ int run_score(const ScoreParams &p, cudaStream_t s)
 
 bool score_supported(const ScoreParams &p)
 {
-    return score_tc_supported(p) || simt_smem(p.Gs, p.H, p.r) <= 227 * 1024;
+    return score_tc_supported(p) || tc_chunk_layers(p) > 0 || simt_smem(p.Gs, p.H, p.r) <= 227 * 1024;
 }
 
 } // namespace

@@ -68,13 +68,15 @@ struct ScoreParams {
     const float *beta;           // [B][T][Gtot][H] or nullptr
     const int32_t *q_pos;        // [T] or nullptr (scan mode only)
     const int32_t *gather_idx;   // [B][L_out] or nullptr (gather mode)
-    float *scores;               // [B][T][Gs][L_out]
+    float *scores;               // [B][T][Gout][L_out]: layer l of the launch -> row gout0 + l
     int *status;
     int lat_t, abs_t;
     int B, T, Gtot, g0, Gs, H, r;
     int L_lat;                   // cached tokens per sequence
     int L_out;                   // positions per score row (scan: L_lat; gather: m)
     int n_gather;                // valid gathered positions (gather mode)
+    int Gout = 0;                // score rows per (sequence, query); 0 = Gs
+    int gout0 = 0;               // first of them written by this launch
 };
 cudaError_t launch_score_simt(const ScoreParams &p, cudaStream_t s);
 bool score_tc_supported(const ScoreParams &p);

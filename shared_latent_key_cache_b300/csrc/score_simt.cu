@@ -93,7 +93,7 @@ __global__ void __launch_bounds__(kTok) score_simt_kernel(const ScoreParams p)
     if (pos >= Lv)
         return;
     const float *c = cs + threadIdx.x * rp;
-    float *out = p.scores + bt * p.Gs * static_cast<int64_t>(p.L_out) + pos;
+    float *out = p.scores + (static_cast<int64_t>(bt) * (p.Gout ? p.Gout : p.Gs) + p.gout0) * p.L_out + pos;
     for (int l = 0; l < p.Gs; ++l) {
         float u = 0.f;
         for (int h = 0; h < p.H; ++h) {

@@ -593,7 +593,8 @@ __global__ void __launch_bounds__(Roles<kGather>::kThreads, 1)
                 const int pos = w.tile * kTileM + row;
                 const bool valid = pos < w.Lv;
                 const float sc = sc_cur;
-                float *out = p.scores + (w.bt * Gs + l0) * static_cast<int64_t>(p.L_out) + pos;
+                float *out = p.scores + (w.bt * (p.Gout ? p.Gout : Gs) + p.gout0 + l0) *
+                                            static_cast<int64_t>(p.L_out) + pos;
                 const uint32_t tacc = tq + static_cast<uint32_t>(acc * kAccStride);
 
                 auto finish = [&](int lay, float u) {

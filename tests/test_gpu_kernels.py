@@ -97,7 +97,8 @@ def test_score_tensor_core(li, orc, dt, L):
 
 
 @pytest.mark.parametrize("dt", ["bf16", "fp8"])
-@pytest.mark.parametrize("G,H,r", [(1, 64, 192), (3, 64, 128), (2, 128, 64), (4, 32, 256), (8, 16, 64)])
+@pytest.mark.parametrize("G,H,r", [(1, 64, 192), (3, 64, 128), (2, 128, 64), (4, 32, 256), (8, 16, 64),
+                                   (8, 64, 192), (5, 64, 128), (3, 128, 64)])
 def test_score_tensor_core_shapes(li, orc, dt, G, H, r):
     g, o = _score_case(li, orc, dt, B=3, T=1, G=G, H=H, r=r, L=777, seed=G * 100 + H)
     assert_scores_close(g, o, RTOL[dt])
@@ -330,6 +331,19 @@ def test_hs_matches_oracle(li, orc, dt):
     w = li_inputs.spec("fp8_128k_hs", B=2, L=3000, m=512, k=128, lat_dtype=dt)
     x = li_inputs.make_workload(w, seed=4)
     _hs_check(li, orc, x, 512, 128, dt)
+
+
+def test_hs_eight_layer_group(li, orc):
+    """G = 8 at H = 64: the group scan and the followers' rescoring exceed one
+    tensor-core tile (256 columns) and run in chunks of four layers."""
+    w = li_inputs.spec("fp8_128k_hs", B=2, L=2500, G=8, m=512, k=128)
+    x = li_inputs.make_workload(w, seed=12)
+    _hs_check(li, orc, x, 512, 128, "fp8")
+    qa, qs = li.absorb_queries(_dev(x["q"]), _dev(x["D"]), "fp8")
+    s = li.score_group(_dev(x["latent"]), _dev(x["lat_scale"]), qa, qs, _dev(x["w"]))
+    _sync_ok(li)
+    o = orc.score(x["latent"], x["lat_scale"], orc.absorb(x["q"], x["D"]), x["w"])
+    assert_scores_close(s.cpu().numpy(), o, RTOL["fp8"])
 
 
 def test_hs_budget_at_least_context_is_full_latentindex(li, orc):
