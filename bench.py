@@ -68,6 +68,22 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(x: float, ws: int, device="cpu") -> float:
+    """The largest of every rank's x (the job's time is its slowest rank's)."""
+    if ws <= 1:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], device=device, dtype=torch.float64)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(bytes_per_step: int, ws: int, ms_per_step: float) -> float:
+    """GB/s of the whole job: every rank's replica steps a batch of its own
+    (weak scaling), so the bytes of all ranks over the slowest rank's time."""
+    return bytes_per_step * ws / (ms_per_step * 1e-3) / 1e9
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -342,12 +358,9 @@ def run_ours(a, w):
     if st != 0:
         raise RuntimeError(li.li_status_string(st))
     step_ms = sum(ev0[i].elapsed_time(ev1[i]) for i in range(K))
-    tot = torch.tensor([step_ms], device=dev, dtype=torch.float64)
-    if ws > 1:
-        torch.distributed.all_reduce(tot, op=torch.distributed.ReduceOp.MAX)
-    ms_per_step = float(tot.item()) / K
+    ms_per_step = max_over_ranks(step_ms, ws, dev) / K
     sb = step_bytes(w)
-    value = sb["total"] * ws / (ms_per_step * 1e-3) / 1e9
+    value = whole_job_rate(sb["total"], ws, ms_per_step)
 
     # Per-kernel breakdown (and the scan's duration for the roofline): a second
     # timed run of the same steps with an event between the kernels.
@@ -417,11 +430,7 @@ def run_ours(a, w):
     st_ = li.li_device_status(stream)
     if st_ != 0:
         raise RuntimeError(li.li_status_string(st_))
-    e2e_ms = ev_start.elapsed_time(ev_end) / E
-    e2e_t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-    if ws > 1:
-        torch.distributed.all_reduce(e2e_t, op=torch.distributed.ReduceOp.MAX)
-    e2e_ms = float(e2e_t.item())
+    e2e_ms = max_over_ranks(ev_start.elapsed_time(ev_end) / E, ws, dev)
     h2d = q_h.numel() * q_h.element_size() + w_h.numel() * w_h.element_size()
     d2h = slots[0]["idx_h"].numel() * slots[0]["idx_h"].element_size()
 
@@ -478,7 +487,7 @@ def run_ours(a, w):
                               "stop the launch overlap, so the three sum to more than latency_us)",
             "step_bytes": sb,
             "wall_s_timed": t_wall,
-            "e2e": {"value": sb["total"] * ws / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+            "e2e": {"value": whole_job_rate(sb["total"], ws, e2e_ms), "unit": "GB/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                     "steps": E, "streams": NS,
                     "timing": "whole run of E steps between two events; steps alternate between two "
