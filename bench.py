@@ -113,10 +113,16 @@ def step_bytes(w) -> dict:
 
 
 def source_hash(paths) -> str:
+    """Hash of the code of `paths` with comments and blank space removed, so
+    that only a change that can change the compiled kernel changes it."""
+    import re
     h = hashlib.sha256()
     for p in paths:
-        with open(os.path.join(ROOT, p), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, p)) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

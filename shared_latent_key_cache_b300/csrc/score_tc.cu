@@ -31,14 +31,13 @@
 //                   latent with 16-byte cp.async into the swizzled layout TMA
 //                   would write, several tiles in flight per thread
 //   8 warps         epilogue, two per TMEM lane quarter (warp % 4), each
-//                   owning 128 accumulator columns (two layers at H = 64): all
-//                   four 32-column TMEM loads in flight, the accumulator
-//                   released as soon as they land, then ReLU, weighted head
-//                   sums with packed fp32 FMA, per-token scale (prefetched one
-//                   tile ahead) and one coalesced store per layer.  (Sixteen
-//                   warps of 64 columns spent more issue slots on per-tile
-//                   bookkeeping than on the arithmetic: the epilogue's issue
-//                   rate, not HBM, set the tile period.)
+//                   owning 128 accumulator columns (two layers at H = 64): two
+//                   64-column TMEM loads in flight, the accumulator released
+//                   as soon as they land, then ReLU, weighted head sums with
+//                   packed fp32 FMA, per-token scale (prefetched one tile
+//                   ahead) and one coalesced store per layer.  (Sixteen warps
+//                   of 64 columns, or two groups of eight taking alternate
+//                   tiles, measured the same time.)
 // The two TMEM accumulators (2 x 256 columns) are double-buffered so the
 // epilogue of tile i overlaps the MMAs of tile i+1 and the loads of the tiles
 // after it.
