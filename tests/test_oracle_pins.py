@@ -451,3 +451,32 @@ def test_planted_reversed_rotation_fails_frequency_schedule():
     bad = twin.append_latent(x, P, rR, [-3])[0]          # same as rotating by -3 theta_0
     np.testing.assert_allclose(good[:2], [math.cos(3.0), math.sin(3.0)], atol=1e-12)
     assert abs(bad[1] - math.sin(3.0)) > 0.1
+
+
+def test_two_pass_selection_equals_one_pass(orc):
+    """The long-row top-k of the GPU library selects in two passes: the exact
+    top-k of each segment, then the top-k of the segments' candidates with
+    ties by position.  On the oracle, with heavy ties across segments, the
+    two passes give the one-pass set (the row's top-k lies inside the union
+    of its segments' top-k)."""
+    g = torch.Generator().manual_seed(51)
+    L, seg = 1000, 256
+    rows = [torch.randint(0, 6, (L,), generator=g).double(),
+            torch.randn(L, generator=g, dtype=torch.float64),
+            torch.full((L,), 2.0, dtype=torch.float64)]
+    for s in rows:
+        s = s.numpy()
+        for k in (1, 7, 100, 256):
+            want, _ = orc.topk(s[None], k)
+            cand_pos, cand_val = [], []
+            for a in range(0, L, seg):
+                i, v = orc.topk(s[None, a:a + seg], k)
+                n = min(k, min(seg, L - a))
+                cand_pos.append(i[0, :n] + a)
+                cand_val.append(v[0, :n])
+            cp, cv = np.concatenate(cand_pos), np.concatenate(cand_val)
+            order = np.argsort(cp, kind="stable")        # candidates in position order,
+            cp, cv = cp[order], cv[order]                 # so ties resolve by position
+            j, _ = orc.topk(cv[None], k)
+            got = cp[j[0][j[0] >= 0]]
+            assert sorted(got.tolist()) == sorted(want[0][want[0] >= 0].tolist())
