@@ -157,6 +157,8 @@ size_t li_hs_workspace_size(int B, int G, int L, int m, int k);
  *   idx  [B][G][k] int32 out: per-layer selections (-1 padded)
  *   ws   device workspace of at least li_hs_workspace_size(B, G, L, m, k)
  *        bytes, 256-byte aligned.
+ * Ties at a threshold go to the lower token position (followers: for
+ * m <= 32,768; beyond that to the earlier slot of the candidate list).
  */
 int li_hs_select(const void *latent, int lat_t, const float *lat_scale,
                  const void *q_abs, int abs_t, const float *q_abs_scale,
