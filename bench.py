@@ -112,6 +112,24 @@ def step_bytes(w) -> dict:
     return b
 
 
+def scan_bytes(w) -> int:
+    """Algorithmic bytes of one group-scan launch: the latent (and its fp8 row
+    scales) read once, the absorbed queries (stored in the latent's type) and
+    the head weights; scores are the launch's output and are not counted."""
+    esz = {"f32": 4, "bf16": 2, "fp8": 1}[w.lat_dtype]
+    return (w.B * w.L * (w.r * esz + (4 if w.lat_dtype == "fp8" else 0)) +
+            w.B * w.T * w.G * w.H * w.r * esz + w.B * w.T * w.G * w.H * 4)
+
+
+def scan_flops(w, q_pos=None) -> int:
+    """2 * G * H * r flops per (query, visible token) pair."""
+    if q_pos is not None:
+        pairs = w.B * sum(min(int(t) + 1, w.L) for t in q_pos)
+    else:
+        pairs = w.B * w.T * w.L
+    return 2 * pairs * w.G * w.H * w.r
+
+
 def source_hash(paths) -> str:
     """Hash of the code of `paths` with comments and blank space removed, so
     that only a change that can change the compiled kernel changes it."""
@@ -447,29 +465,23 @@ def run_ours(a, w):
 
     # ---- roofline of the dominant kernel (the group scan)
     pk = peaks()
-    esz = {"f32": 4, "bf16": 2, "fp8": 1}[w.lat_dtype]
-    scan_bytes = (B * L * (r * esz + (4 if w.lat_dtype == "fp8" else 0)) +
-                  q_abs.numel() * q_abs.element_size() + x["w"].numel() * 4)
-    if x["q_pos"] is not None:
-        pairs = B * int((x["q_pos"].long() + 1).clamp(max=L).sum().item())   # causal (query, token) pairs
-    else:
-        pairs = B * T * L
-    scan_flops = 2 * pairs * G * H * r
+    sbytes = scan_bytes(w)
+    sflops = scan_flops(w, x["q_pos"].tolist() if x["q_pos"] is not None else None)
     if T > 1:
         # prefill-shaped scoring is a dense contraction: tensor-bound
-        achieved = scan_flops / (score_us * 1e-6) / 1e12
+        achieved = sflops / (score_us * 1e-6) / 1e12
         peak = pk["bf16_tflops_sustained"] or pk["bf16_tflops"]
         roof = {"kernel": "score_tc_kernel (causal prefill scoring)", "bound": "tensor",
                 "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                 "traffic": None, "peak_source": pk["source"] + " cuBLAS bf16, sustained (a ~35 ms kernel)",
-                "algorithmic_bytes_per_launch": scan_bytes, "flops_per_launch": scan_flops}
+                "algorithmic_bytes_per_launch": sbytes, "flops_per_launch": sflops}
     else:
-        achieved = scan_bytes / (score_us * 1e-6) / 1e9
+        achieved = sbytes / (score_us * 1e-6) / 1e9
         tr = ncu_traffic(w.name)
         roof = {"kernel": "score_tc_kernel (group scan)", "bound": "hbm", "achieved": achieved,
                 "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
                 "traffic": tr, "peak_source": pk["source"] + " copy bandwidth",
-                "algorithmic_bytes_per_launch": scan_bytes, "flops_per_launch": scan_flops}
+                "algorithmic_bytes_per_launch": sbytes, "flops_per_launch": sflops}
 
     if rank == 0:
         cb = None
