@@ -512,7 +512,7 @@ def run_ours(a, w):
                               "streams so copies overlap kernels; no L2 flush (each step streams the "
                               "whole latent cache)",
                     "resident": "latent cache and decoders (device state across decode steps)"},
-            "gpu_launches": 3 * K,
+            "gpu_launches": (4 if tws is not None else 3) * K,   # absorb, scan, top-k (two passes for long rows)
             "roofline": roof,
             "clocks": clocks,
             "cpu_baseline": cb,
