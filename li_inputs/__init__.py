@@ -39,7 +39,7 @@ import math
 import torch
 
 __all__ = ["Workload", "WORKLOADS", "spec", "make_workload", "make_latent",
-           "make_absorbed_queries", "quantize_rows_fp8", "FP8_MAX"]
+           "make_absorbed_queries", "make_rotary_decoders", "quantize_rows_fp8", "FP8_MAX"]
 
 FP8_MAX = 448.0
 
@@ -174,6 +174,42 @@ def make_append_inputs(B: int, dm: int, r: int, dtype: str = "bf16", seed: int =
     P = torch.randn(r, dm, generator=_gen(seed, 22, "cpu")) / dm ** 0.5
     dt = {"f32": torch.float32, "bf16": torch.bfloat16}[dtype]
     return x.to(dt).to(device), P.to(dt).to(device)
+
+
+def make_rotary_decoders(G: int, r: int, rR: int, d: int, dR: int, seed: int = 0):
+    """Random decoders whose RoPE part obeys the rotary-structure constraint
+    (summary page, eqs. (3)-(4)), as raw draws plus their storage.
+
+    Key RoPE pair j (of dR/2) and latent RoPE pair i (of rR/2) are coupled by
+    one complex number (a_re + i a_im)[l][j][i] when j * rR == i * dR (their
+    rotary frequencies are equal) and not at all otherwise; the NoPE block maps
+    the r - rR latent NoPE values to the d - dR key NoPE values.  Draws:
+    a_re, a_im, DN ~ N(0, 1/r), rounded to bfloat16 so that the f32 and bf16
+    storages hold exactly the drawn values.
+
+    Returns a dict with a_re, a_im [G][dR/2][rR/2], DN [G][d - dR][r - rR]
+    (float64 tensors) and D [G][r][d] float32, the decoders in the library's
+    storage orientation (k = D_l^T c): rows < rR / columns < dR carry the
+    2 x 2 blocks [[a, -b], [b, a]] transposed, rows >= rR / columns >= dR
+    carry DN transposed, the rest is zero."""
+    g = torch.Generator().manual_seed((int(seed) * 1_000_003 + 31 * 7919 + 17) & 0x7FFF_FFFF_FFFF)
+    s = 1.0 / math.sqrt(r)
+    bf = lambda t: t.to(torch.bfloat16).double()
+    a_re = bf(torch.randn(G, dR // 2, rR // 2, generator=g) * s)
+    a_im = bf(torch.randn(G, dR // 2, rR // 2, generator=g) * s)
+    DN = bf(torch.randn(G, d - dR, r - rR, generator=g) * s)
+    D = torch.zeros(G, r, d, dtype=torch.float64)
+    for j in range(dR // 2):
+        for i in range(rR // 2):
+            if j * rR != i * dR:
+                continue
+            a, b = a_re[:, j, i], a_im[:, j, i]
+            # key rows (2j, 2j+1) x latent columns (2i, 2i+1) = [[a, -b], [b, a]],
+            # stored transposed: D[latent][key]
+            D[:, 2 * i, 2 * j], D[:, 2 * i + 1, 2 * j] = a, -b
+            D[:, 2 * i, 2 * j + 1], D[:, 2 * i + 1, 2 * j + 1] = b, a
+    D[:, rR:, dR:] = DN.transpose(1, 2)
+    return {"a_re": a_re, "a_im": a_im, "DN": DN, "D": D.float().contiguous()}
 
 
 def make_workload(w: Workload | str, seed: int = 0, device="cpu") -> dict:

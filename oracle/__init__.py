@@ -64,8 +64,12 @@ def lib():
         L.or_hs.argtypes = [P, I, I, I, I, I, P, P, I]
         L.or_native_score.argtypes = [P, I, P, P, P, I, I, I, I, P, I]
         L.or_append_latent.argtypes = [P, I, P, I, I, I, I, I, ctypes.c_double, P, P, I]
+        L.or_rope_rotate.argtypes = [P, I64, I, I, ctypes.c_double, P]
+        L.or_rotary_decoder.argtypes = [P, P, I, I, P]
+        L.or_rope_keys.argtypes = [P, I, P, I, I, I, I, I, P, P, P, I, I, I, ctypes.c_double, P, P, I]
         for f in ("or_decode_rows", "or_absorb", "or_reconstruct_keys", "or_score", "or_topk",
-                  "or_hs", "or_native_score", "or_append_latent"):
+                  "or_hs", "or_native_score", "or_append_latent", "or_rope_rotate",
+                  "or_rotary_decoder", "or_rope_keys"):
             getattr(L, f).restype = None
         _lib = L
     return _lib
@@ -219,6 +223,50 @@ def append_latent(x, P, rR: int, pos, base: float = 10000.0, nthreads: int | Non
     out = np.empty((B, r), dtype=np.float64)
     lib().or_append_latent(_p(xa), _code(xa), _p(Pa), _code(Pa), B, dm, r, rR, float(base), _p(pa),
                            _p(out), nthreads or default_threads())
+    return out
+
+
+def rope_rotate(v, nR: int, pos, base: float = 10000.0) -> np.ndarray:
+    """Rotary encoding of the first nR entries of each row of v [n][dim] by its
+    position pos [n] (R_t of eq. (4) on a key's RoPE part; Q_t on a latent's
+    RoPE branch).  Returns a new fp64 array."""
+    out = np.array(_f64(v), dtype=np.float64, copy=True, order="C")
+    n, dim = out.shape
+    pa = np.ascontiguousarray(_np(pos), dtype=np.int32).reshape(-1)
+    assert pa.size == n and nR % 2 == 0 and nR <= dim
+    lib().or_rope_rotate(_p(out), n, dim, nR, float(base), _p(pa))
+    return out
+
+
+def rotary_decoder(a_re, a_im, dR: int, rR: int) -> np.ndarray:
+    """RoPE part D^R [dR][rR] of a decoder under eq. (4), R_t D^R = D^R Q_t:
+    key pair j and latent pair i are coupled by the complex number
+    a_re[j][i] + i a_im[j][i] when their rotary frequencies are equal
+    (j * rR == i * dR), and not at all otherwise.  a_re, a_im [dR/2][rR/2]."""
+    ar = np.ascontiguousarray(_f64(a_re)).reshape(dR // 2, rR // 2)
+    ai = np.ascontiguousarray(_f64(a_im)).reshape(dR // 2, rR // 2)
+    out = np.empty((dR, rR), dtype=np.float64)
+    lib().or_rotary_decoder(_p(ar), _p(ai), dR, rR, _p(out))
+    return out
+
+
+def rope_keys(x, P, rR: int, DR, DN, pos, bias=None, base: float = 10000.0,
+              nthreads: int | None = None) -> np.ndarray:
+    """Eq. (3) the native way: per-layer keys [R_t D^R_l P_R^T x ; D^N_l P_N^T x + b_l]
+    of the token of each sequence at position pos [B].  x [B][dm], P [r][dm],
+    DR [G][dR][rR], DN [G][dN][r - rR], bias [G][dN] or None -> keys [G][B][dR + dN]."""
+    xa, Pa = np.ascontiguousarray(_np(x)), np.ascontiguousarray(_np(P))
+    B, dm = xa.shape
+    r = Pa.shape[0]
+    DRa, DNa = _f64(DR), _f64(DN)
+    G, dR, rR2 = DRa.shape
+    _, dN, rN = DNa.shape
+    assert rR2 == rR and rN == r - rR and r <= 1024
+    ba = _f64(bias)
+    pa = np.ascontiguousarray(_np(pos), dtype=np.int32).reshape(-1)
+    out = np.empty((G, B, dR + dN), dtype=np.float64)
+    lib().or_rope_keys(_p(xa), _code(xa), _p(Pa), _code(Pa), B, dm, r, rR, _p(DRa), _p(DNa), _p(ba),
+                       G, dR, dN, float(base), _p(pa), _p(out), nthreads or default_threads())
     return out
 
 

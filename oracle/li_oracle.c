@@ -20,6 +20,9 @@
  *   [S] Methodology, "Shared Latent Cache", eqs. (1)-(2): the latent of a
  *        token is built from the anchor layer's hidden state x as
  *        z^N = P_N^T x, z^R = Q_t P_R^T x, c = [z^R; z^N].
+ *   [S] Methodology, "Layer-specific Key Reconstruction", eqs. (3)-(4): a
+ *        decoder's RoPE part satisfies R_t D^R = D^R Q_t through complex
+ *        linear combinations within each rotary frequency.
  *
  * Notation.  A decoder is stored as D_l with shape r x d (r = latent rank,
  * d = per-layer indexer key width), so the per-layer key of eq. (3) is
@@ -307,6 +310,92 @@ void or_append_latent(const void *x, int x_t, const void *P, int P_t, int B, int
             const double re = cb[2 * i], im = cb[2 * i + 1];
             cb[2 * i] = re * cos(ang) - im * sin(ang);
             cb[2 * i + 1] = re * sin(ang) + im * cos(ang);
+        }
+    }
+}
+
+/* Rotary position encoding applied to the first nR entries of each of n rows
+ * of width dim: pair j (v_2j, v_2j+1) of row i is read as a complex number and
+ * multiplied by exp(i pos[i] theta_j), theta_j = base^(-2j/nR).  This is R_t
+ * of eq. (4) of [S] on the RoPE part of a per-layer key (and the same
+ * schedule as Q_t of eq. (1) on the latent's RoPE branch, with nR = rR). */
+void or_rope_rotate(double *v, int64_t n, int dim, int nR, double base, const int32_t *pos)
+{
+    for (int64_t i = 0; i < n; i++) {
+        double *row = v + i * dim;
+        for (int j = 0; j < nR / 2; j++) {
+            const double ang = (double)pos[i] * pow(base, -2.0 * j / nR);
+            const double re = row[2 * j], im = row[2 * j + 1];
+            row[2 * j] = re * cos(ang) - im * sin(ang);
+            row[2 * j + 1] = re * sin(ang) + im * cos(ang);
+        }
+    }
+}
+
+/* The RoPE part of a decoder under the rotary-structure constraint of eq. (4)
+ * of [S], R_t D^R = D^R Q_t, "enforced through complex linear combinations
+ * within each rotary frequency".  Key pair j (of dR/2; frequency
+ * base^(-2j/dR)) and latent pair i (of rR/2; frequency base^(-2i/rR)) are
+ * coupled only when the two frequencies are equal, i.e. j * rR == i * dR,
+ * and then by the complex number a + ib = (are, aim)[j][i]: the 2 x 2 block
+ * [[a, -b], [b, a]], which commutes with every rotation.  Other entries of
+ * the coefficient arrays [dR/2][rR/2] are ignored.
+ *   DR [dR][rR] fp64 out (key = DR z, the summary page's orientation) */
+void or_rotary_decoder(const double *are, const double *aim, int dR, int rR, double *DR)
+{
+    memset(DR, 0, sizeof(double) * (size_t)dR * (size_t)rR);
+    for (int j = 0; j < dR / 2; j++) {
+        for (int i = 0; i < rR / 2; i++) {
+            if ((int64_t)j * rR != (int64_t)i * dR)
+                continue;
+            const double a = are[(int64_t)j * (rR / 2) + i], b = aim[(int64_t)j * (rR / 2) + i];
+            DR[(int64_t)(2 * j) * rR + 2 * i] = a;
+            DR[(int64_t)(2 * j) * rR + 2 * i + 1] = -b;
+            DR[(int64_t)(2 * j + 1) * rR + 2 * i] = b;
+            DR[(int64_t)(2 * j + 1) * rR + 2 * i + 1] = a;
+        }
+    }
+}
+
+/* Eq. (3) of [S] evaluated the native way, as per-layer indexer keys with
+ * their own rotary encoding: for the token of sequence b at position pos[b],
+ *   k^R = R_t (D^R_l P_R^T x)        (rotated after decoding)
+ *   k^N = D^N_l P_N^T x + b_l
+ *   key = [k^R ; k^N]   (d = dR + dN values)
+ * which eqs. (1), (4) and (7) say equals the key decoded from the rotated
+ * latent, D_l c_t with c_t = [Q_t P_R^T x ; P_N^T x].
+ *   x [B][dm] (x_t), P [r][dm] (P_t; rows < rR are P_R^T, the rest P_N^T)
+ *   DR [G][dR][rR], DN [G][dN][r - rR], bias [G][dN] or NULL (all fp64)
+ *   keys [G][B][dR + dN] fp64 out */
+void or_rope_keys(const void *x, int x_t, const void *P, int P_t, int B, int dm, int r, int rR,
+                  const double *DR, const double *DN, const double *bias, int G, int dR, int dN,
+                  double base, const int32_t *pos, double *keys, int nthreads)
+{
+    const int d = dR + dN, rN = r - rR;
+    #pragma omp parallel for num_threads(nthreads) schedule(static)
+    for (int b = 0; b < B; b++) {
+        double z[1024];
+        for (int i = 0; i < r; i++) {
+            double acc = 0.0;
+            for (int j = 0; j < dm; j++)
+                acc += elem(P, P_t, (int64_t)i * dm + j) * elem(x, x_t, (int64_t)b * dm + j);
+            z[i] = acc;                       /* [P_R^T x ; P_N^T x], no rotation yet */
+        }
+        for (int l = 0; l < G; l++) {
+            double *k = keys + ((int64_t)l * B + b) * d;
+            for (int j = 0; j < dR; j++) {
+                double acc = 0.0;
+                for (int i = 0; i < rR; i++)
+                    acc += DR[((int64_t)l * dR + j) * rR + i] * z[i];
+                k[j] = acc;
+            }
+            for (int j = 0; j < dN; j++) {
+                double acc = bias ? bias[(int64_t)l * dN + j] : 0.0;
+                for (int i = 0; i < rN; i++)
+                    acc += DN[((int64_t)l * dN + j) * rN + i] * z[rR + i];
+                k[dR + j] = acc;
+            }
+            or_rope_rotate(k, 1, d, dR, base, pos + b);
         }
     }
 }

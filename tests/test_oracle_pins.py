@@ -480,3 +480,147 @@ def test_two_pass_selection_equals_one_pass(orc):
             j, _ = orc.topk(cv[None], k)
             got = cp[j[0][j[0] >= 0]]
             assert sorted(got.tolist()) == sorted(want[0][want[0] >= 0].tolist())
+
+
+# --------------------------------- rotary-constrained decoders, eqs. (3)-(4)
+
+def _rot_matrix(orc, n, t):
+    """The rotation of `orc.rope_rotate` at position t as an n x n matrix M with M v = rotated v."""
+    rows = orc.rope_rotate(np.eye(n), n, np.full(n, t, dtype=np.int32))   # row i = (M e_i)^T
+    return rows.T
+
+
+@pytest.mark.parametrize("dR,rR", [(8, 8), (8, 16), (64, 64)])
+def test_rotary_decoder_commutes_with_rotation(orc, dR, rR):
+    """Eq. (4): R_t D^R = D^R Q_t for every position t, with R_t the key's and
+    Q_t the latent's rotary encoding (each with its own width)."""
+    rng = np.random.default_rng(41)
+    DR = orc.rotary_decoder(rng.standard_normal((dR // 2, rR // 2)),
+                            rng.standard_normal((dR // 2, rR // 2)), dR, rR)
+    assert np.abs(DR).sum() > 0
+    for t in (1, 7, 1000, 131071):
+        lhs = _rot_matrix(orc, dR, t) @ DR
+        rhs = DR @ _rot_matrix(orc, rR, t)
+        np.testing.assert_allclose(lhs, rhs, rtol=0, atol=1e-12)
+
+
+def test_rotation_matrix_is_the_frequency_schedule(orc):
+    """Pair j of an n-wide rotary encoding turns by t * 10000^(-2j/n): the
+    matrix form used by the eq. (4) pins, checked entry by entry."""
+    n, t = 6, 5
+    M = _rot_matrix(orc, n, t)
+    want = np.zeros((n, n))
+    for j in range(n // 2):
+        a = t * 10000.0 ** (-2.0 * j / n)
+        want[2 * j:2 * j + 2, 2 * j:2 * j + 2] = [[math.cos(a), -math.sin(a)], [math.sin(a), math.cos(a)]]
+    np.testing.assert_allclose(M, want, atol=1e-13)
+
+
+def test_planted_real_block_fails_rotary_constraint(orc):
+    """A decoder block that is a real 2 x 2 matrix but not a complex number
+    ([[a, b], [b, -a]], a reflection) breaks eq. (4)."""
+    a, b = 0.7, -0.4
+    DR = np.array([[a, b], [b, -a]])
+    t = 3
+    lhs = _rot_matrix(orc, 2, t) @ DR
+    rhs = DR @ _rot_matrix(orc, 2, t)
+    assert np.abs(lhs - rhs).max() > 0.1
+
+
+def test_input_generator_rotary_decoders_match_oracle_builder(orc):
+    """The decoders the GPU tests store (li_inputs) have, in their RoPE block,
+    the oracle's eq. (4) decoder of the same draws, and in their NoPE block the
+    drawn DN; the cross blocks are zero."""
+    G, r, rR, d, dR = 3, 40, 16, 24, 8
+    dec = li_inputs.make_rotary_decoders(G, r, rR, d, dR, seed=5)
+    D = dec["D"].double().numpy()
+    for l in range(G):
+        DR = orc.rotary_decoder(dec["a_re"][l], dec["a_im"][l], dR, rR)
+        np.testing.assert_array_equal(D[l, :rR, :dR], DR.T)
+        np.testing.assert_array_equal(D[l, rR:, dR:], dec["DN"][l].numpy().T)
+        assert not D[l, :rR, dR:].any() and not D[l, rR:, :dR].any()
+
+
+def _rotary_case(orc, B=3, dm=40, r=24, rR=8, d=20, dR=8, G=2, H=3, seed=43):
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((B, dm))
+    P = rng.standard_normal((r, dm)) / math.sqrt(dm)
+    DR = np.stack([orc.rotary_decoder(rng.standard_normal((dR // 2, rR // 2)),
+                                      rng.standard_normal((dR // 2, rR // 2)), dR, rR) for _ in range(G)])
+    DN = rng.standard_normal((G, d - dR, r - rR)) / math.sqrt(r)
+    bias = rng.standard_normal((G, d - dR))
+    q = rng.standard_normal((B, 1, G, H, d)) / math.sqrt(d)
+    w = rng.random((B, 1, G, H))
+    D = np.zeros((G, r, d))
+    D[:, :rR, :dR] = DR.transpose(0, 2, 1)
+    D[:, rR:, dR:] = DN.transpose(0, 2, 1)
+    return dict(x=x, P=P, DR=DR, DN=DN, bias=bias, q=q, w=w, D=D, rR=rR, dR=dR, G=G)
+
+
+def _latent_route(orc, c, k, pos, with_bias=True):
+    """Eqs. (1)-(2), (6), (8): score the rotated latent with absorbed queries (+ beta)."""
+    lat = orc.append_latent(c["x"], c["P"], c["rR"], pos)           # [B][r]
+    qabs = orc.absorb(c["q"], c["D"])                               # [B][1][G][H][r]
+    beta = np.einsum("btghn,gn->btgh", c["q"][..., c["dR"]:], c["bias"]) if with_bias else None
+    B = lat.shape[0]
+    # one cached token per sequence: score it with its own sequence's queries
+    return np.stack([orc.score(lat[b:b + 1, None], None, qabs[b:b + 1], c["w"][b:b + 1],
+                               None if beta is None else beta[b:b + 1])[0, 0, :, 0] for b in range(B)])
+
+
+def _key_route(orc, c, pos):
+    """Eq. (3) with eq. (4): per-layer keys rotated after decoding, scored natively."""
+    keys = orc.rope_keys(c["x"], c["P"], c["rR"], c["DR"], c["DN"], pos, bias=c["bias"])  # [G][B][d]
+    B = keys.shape[1]
+    return np.stack([[orc.native_score(keys[l, b:b + 1, None], None, c["q"][b:b + 1, 0, l],
+                                       c["w"][b:b + 1, 0, l])[0, 0] for l in range(c["G"])]
+                     for b in range(B)])
+
+
+@pytest.mark.parametrize("shape", [dict(), dict(r=48, rR=16, d=24, dR=8), dict(r=32, rR=8, d=24, dR=16)])
+def test_rotary_latent_scoring_equals_rope_key_scoring(orc, shape):
+    """Eqs. (1), (3), (4), (6)-(8) end to end: scoring the cached latent, which
+    is rotated once by Q_t, with decoder-absorbed queries and beta gives the
+    scores of the per-layer keys [R_t D^R z^R ; D^N z^N + b] that the native
+    indexer would cache."""
+    c = _rotary_case(orc, **shape)
+    for pos in ([0, 1, 2], [5, 131071, 4096]):
+        pos = np.array(pos, dtype=np.int32)
+        got = _latent_route(orc, c, 0, pos)
+        want = _key_route(orc, c, pos)
+        np.testing.assert_allclose(got, want, rtol=1e-10, atol=1e-12)
+        assert (want > 0).any()
+
+
+def test_planted_reversed_latent_rotation_fails_key_identity(orc):
+    """Rotating the latent by -t (the conjugate of Q_t) breaks the identity."""
+    c = _rotary_case(orc)
+    pos = np.array([9, 300, 77], dtype=np.int32)
+    want = _key_route(orc, c, pos)
+    bad = _latent_route(orc, c, 0, -pos)
+    assert np.abs(bad - want).max() > 1e-3 * np.abs(want).max()
+
+
+def test_planted_dropped_bias_fails_key_identity(orc):
+    c = _rotary_case(orc)
+    pos = np.array([9, 300, 77], dtype=np.int32)
+    assert np.abs(_latent_route(orc, c, 0, pos, with_bias=False) - _key_route(orc, c, pos)).max() > 1e-6
+
+
+def test_rope_key_scores_depend_only_on_relative_position(orc):
+    """With the query's RoPE part rotated by R_s, the score of a key at t
+    depends on s - t only: shifting both positions leaves it unchanged."""
+    c = _rotary_case(orc, B=1)
+    dR = c["dR"]
+    q0 = c["q"].copy()
+
+    def score_at(s, t):
+        q = q0.copy()
+        flat = q.reshape(-1, q.shape[-1])
+        flat[:] = orc.rope_rotate(flat, dR, np.full(flat.shape[0], s, dtype=np.int32))
+        keys = orc.rope_keys(c["x"], c["P"], c["rR"], c["DR"], c["DN"], np.array([t], dtype=np.int32),
+                             bias=c["bias"])
+        return np.array([orc.native_score(keys[l, :, None], None, q[:, 0, l], c["w"][:, 0, l])[0, 0]
+                         for l in range(c["G"])])
+    for s, t, shift in ((10, 3, 1000), (5000, 4999, 77), (0, 0, 131000)):
+        np.testing.assert_allclose(score_at(s, t), score_at(s + shift, t + shift), rtol=1e-9, atol=1e-12)
