@@ -31,6 +31,11 @@
  *    ("fn") codes with one fp32 scale per row: value = scale * decode(code).
  *    Scales must be >= 0 and finite.
  *  - Calls are reentrant; concurrent calls on different streams are safe.
+ *  - The library caches, per device, the device addresses of its own device
+ *    variables (the status word; the scratch array of li_hs_select_noalloc),
+ *    looked up on first use.  cudaDeviceReset() on a device invalidates them:
+ *    do not call into the library on that device after a reset in the same
+ *    process.
  */
 #ifndef LI_B300_H
 #define LI_B300_H
@@ -165,6 +170,24 @@ int li_hs_select(const void *latent, int lat_t, const float *lat_scale,
                  const float *w, const float *beta,
                  int B, int G, int H, int r, int L, int m, int k,
                  int32_t *cand, int32_t *idx, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * li_hs_select with per-launch timing (a diagnostic entry point; the pages
+ * have no counterpart).  Same arguments, work and results as li_hs_select,
+ * plus `events`: six caller-created cudaEvent_t handles.  events[i] is
+ * recorded on `stream` before launch i of the selection and events[5] after
+ * the last one: 0 anchor scan, 1 anchor top-m (candidates), 2 anchor top-k,
+ * 3 follower rescoring of the candidates, 4 follower top-k (with G = 1 the
+ * last three intervals are empty).  Recording an event between two launches
+ * ends their programmatic launch overlap, so the intervals add up to a little
+ * more than an unprofiled call.  LI_ERR_INVALID_ARG when events is NULL.
+ */
+int li_hs_select_profiled(const void *latent, int lat_t, const float *lat_scale,
+                          const void *q_abs, int abs_t, const float *q_abs_scale,
+                          const float *w, const float *beta,
+                          int B, int G, int H, int r, int L, int m, int k,
+                          int32_t *cand, int32_t *idx, void *ws, size_t ws_bytes,
+                          void *const *events, void *stream);
 
 /*
  * Hierarchical selection without a caller workspace.  The paper has no

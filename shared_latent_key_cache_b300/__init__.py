@@ -23,7 +23,8 @@ __all__ = [
     "LI_F32", "LI_BF16", "LI_FP8_E4M3", "LiError", "lib", "library_path",
     "li_version", "li_status_string", "li_absorb_queries", "li_score_group", "li_topk",
     "li_topk_workspace_size",
-    "li_hs_workspace_size", "li_hs_select", "li_hs_select_noalloc", "li_native_score",
+    "li_hs_workspace_size", "li_hs_select", "li_hs_select_profiled", "li_hs_select_noalloc",
+    "li_native_score",
     "li_device_status", "li_selftest_wait_timeout", "li_append_latent", "append_latent",
     "absorb_queries", "score_group", "topk", "hs_select", "native_score", "device_status",
 ]
@@ -61,10 +62,11 @@ def _load():
     L.li_hs_select.argtypes = [P, I, P, P, I, P, P, P, I, I, I, I, I, I, I, P, P, P, S, P]
     L.li_native_score.argtypes = [P, I, P, P, I, P, P, I, I, I, I, P, P]
     L.li_hs_select_noalloc.argtypes = [P, I, P, P, I, P, P, P, I, I, I, I, I, I, I, P, P, P]
+    L.li_hs_select_profiled.argtypes = [P, I, P, P, I, P, P, P, I, I, I, I, I, I, I, P, P, P, S, P, P]
     L.li_device_status.argtypes = [P]
     L.li_selftest_wait_timeout.argtypes = [ctypes.c_uint, P]
     L.li_append_latent.argtypes = [P, I, P, I, P, I, I, I, I, ctypes.c_float, P, I, P, I, P]
-    for f in ("li_absorb_queries", "li_score_group", "li_topk", "li_hs_select",
+    for f in ("li_absorb_queries", "li_score_group", "li_topk", "li_hs_select", "li_hs_select_profiled",
               "li_native_score", "li_device_status", "li_hs_select_noalloc",
               "li_selftest_wait_timeout", "li_append_latent"):
         getattr(L, f).restype = I
@@ -171,6 +173,18 @@ def li_hs_select(latent, lat_scale, q_abs, q_abs_scale, w, m: int, k: int, cand,
         _ptr(latent), _dtype_code(latent), _ptr(lat_scale), _ptr(q_abs), _dtype_code(q_abs),
         _ptr(q_abs_scale), _ptr(w), _ptr(beta), B, G, H, r, L, m, k, _ptr(cand), _ptr(idx),
         _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
+
+
+def li_hs_select_profiled(latent, lat_scale, q_abs, q_abs_scale, w, m: int, k: int, cand, idx, ws,
+                          events, beta=None, stream=None) -> int:
+    """li_hs_select with six torch.cuda.Event objects recorded around its five launches."""
+    B, L, r = latent.shape
+    _, _, G, H, _ = q_abs.shape
+    arr = (ctypes.c_void_p * 6)(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    return _lib.li_hs_select_profiled(
+        _ptr(latent), _dtype_code(latent), _ptr(lat_scale), _ptr(q_abs), _dtype_code(q_abs),
+        _ptr(q_abs_scale), _ptr(w), _ptr(beta), B, G, H, r, L, m, k, _ptr(cand), _ptr(idx),
+        _ptr(ws), ws.numel() * ws.element_size(), arr, _stream(stream))
 
 
 def li_hs_select_noalloc(latent, lat_scale, q_abs, q_abs_scale, w, m: int, k: int, cand, idx,

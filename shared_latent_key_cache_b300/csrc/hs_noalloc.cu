@@ -64,11 +64,13 @@ int li_hs_select_noalloc(const void *latent, int lat_t, const float *lat_scale, 
                          int B, int G, int H, int r, int L, int m, int k, int32_t *cand,
                          int32_t *idx, void *stream)
 {
-    // arguments first, without touching CUDA
-    if (!latent || !q_abs || !w || !cand || !idx)
-        return LI_ERR_INVALID_ARG;
-    if (B <= 0 || G <= 0 || H <= 0 || r <= 0 || L <= 0 || m <= 0 || k <= 0 || m < k)
-        return LI_ERR_INVALID_ARG;
+    // the same argument checks as li_hs_select first, without touching CUDA, so
+    // that both entry points report the same status for the same bad call;
+    // only then the size limit of the built-in scratch
+    const int st = li::hs_check_args(latent, lat_t, lat_scale, q_abs, abs_t, q_abs_scale, w, beta, B,
+                                     G, H, r, L, m, k, cand, idx);
+    if (st != LI_OK)
+        return st;
     const size_t need = li_hs_workspace_size(B, G, L, m, k);
     if (need == 0)
         return LI_ERR_INVALID_ARG;

@@ -325,19 +325,38 @@ size_t li_hs_workspace_size(int B, int G, int L, int m, int k)
     return anchor + cvals + fol + topk_two_pass_bytes(B, L, m);
 }
 
-int li_hs_select(const void *latent, int lat_t, const float *lat_scale, const void *q_abs, int abs_t,
-                 const float *q_abs_scale, const float *w, const float *beta, int B, int G, int H,
-                 int r, int L, int m, int k, int32_t *cand, int32_t *idx, void *ws, size_t ws_bytes,
-                 void *stream)
+} // extern "C"
+
+namespace li {
+
+int hs_check_args(const void *latent, int lat_t, const float *lat_scale, const void *q_abs,
+                  int abs_t, const float *q_abs_scale, const float *w, const float *beta, int B,
+                  int G, int H, int r, int L, int m, int k, const int32_t *cand, const int32_t *idx)
 {
-    int st = check_score_args(latent, lat_t, lat_scale, q_abs, abs_t, q_abs_scale, w, beta, nullptr,
-                              cand, B, 1, G, H, r, L);
+    const int st = check_score_args(latent, lat_t, lat_scale, q_abs, abs_t, q_abs_scale, w, beta,
+                                    nullptr, cand, B, 1, G, H, r, L);
     if (st != LI_OK)
         return st;
     if (!idx || m <= 0 || k <= 0 || m < k)
         return LI_ERR_INVALID_ARG;
     if (!aligned16(idx))
         return LI_ERR_ALIGNMENT;
+    return LI_OK;
+}
+
+namespace {
+
+// The five launches of hierarchical selection; when `ev` is given, ev[i] is
+// recorded on the stream before launch i and ev[5] after the last one.
+int hs_select_impl(const void *latent, int lat_t, const float *lat_scale, const void *q_abs,
+                   int abs_t, const float *q_abs_scale, const float *w, const float *beta, int B,
+                   int G, int H, int r, int L, int m, int k, int32_t *cand, int32_t *idx, void *ws,
+                   size_t ws_bytes, void *stream, cudaEvent_t const *ev)
+{
+    int st = hs_check_args(latent, lat_t, lat_scale, q_abs, abs_t, q_abs_scale, w, beta, B, G, H, r,
+                           L, m, k, cand, idx);
+    if (st != LI_OK)
+        return st;
     const size_t need = li_hs_workspace_size(B, G, L, m, k);
     if (!ws || ws_bytes < need)
         return LI_ERR_WORKSPACE;
@@ -391,11 +410,17 @@ int li_hs_select(const void *latent, int lat_t, const float *lat_scale, const vo
     a.status = f.status = status;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
+    auto mark = [&](int i) {
+        if (ev != nullptr && ev[i] != nullptr)
+            cudaEventRecord(ev[i], s);
+    };
     // 1. anchor scores over all L positions
+    mark(0);
     st = run_score(a, s);
     if (st != LI_OK)
         return st;
     // 2. anchor top-m -> candidate set (and its scores)
+    mark(1);
     TopkParams t{};
     t.scores = anchor;
     t.rows = B;
@@ -416,6 +441,7 @@ int li_hs_select(const void *latent, int lat_t, const float *lat_scale, const vo
     if (st != LI_OK)
         return st;
     // 3. the anchor's own top-k, inside its candidates
+    mark(2);
     TopkParams ta = t;
     ta.scores = cvals;
     ta.in_stride = m;
@@ -427,20 +453,57 @@ int li_hs_select(const void *latent, int lat_t, const float *lat_scale, const vo
     ta.map = cand;
     ta.map_stride = m;
     st = cuda_status(launch_topk(ta, s));
-    if (st != LI_OK || G == 1)
+    if (st != LI_OK || G == 1) {
+        mark(3);
+        mark(4);
+        mark(5);
         return st;
+    }
     // 4. followers rescore the candidate rows of the latent
+    mark(3);
     st = run_score(f, s);
     if (st != LI_OK)
         return st;
     // 5. followers' top-k inside the candidates
+    mark(4);
     TopkParams tf = ta;
     tf.scores = fol;
     tf.rows = static_cast<int64_t>(B) * (G - 1);
     tf.rows_per_group = G - 1;
     tf.group_stride = G;
     tf.row_offset = 1;
-    return cuda_status(launch_topk(tf, s));
+    st = cuda_status(launch_topk(tf, s));
+    mark(5);
+    return st;
+}
+
+} // namespace
+} // namespace li
+
+extern "C" {
+
+int li_hs_select(const void *latent, int lat_t, const float *lat_scale, const void *q_abs, int abs_t,
+                 const float *q_abs_scale, const float *w, const float *beta, int B, int G, int H,
+                 int r, int L, int m, int k, int32_t *cand, int32_t *idx, void *ws, size_t ws_bytes,
+                 void *stream)
+{
+    return hs_select_impl(latent, lat_t, lat_scale, q_abs, abs_t, q_abs_scale, w, beta, B, G, H, r,
+                          L, m, k, cand, idx, ws, ws_bytes, stream, nullptr);
+}
+
+int li_hs_select_profiled(const void *latent, int lat_t, const float *lat_scale, const void *q_abs,
+                          int abs_t, const float *q_abs_scale, const float *w, const float *beta,
+                          int B, int G, int H, int r, int L, int m, int k, int32_t *cand,
+                          int32_t *idx, void *ws, size_t ws_bytes, void *const *events,
+                          void *stream)
+{
+    if (!events)
+        return LI_ERR_INVALID_ARG;
+    cudaEvent_t ev[6];
+    for (int i = 0; i < 6; ++i)
+        ev[i] = static_cast<cudaEvent_t>(events[i]);
+    return hs_select_impl(latent, lat_t, lat_scale, q_abs, abs_t, q_abs_scale, w, beta, B, G, H, r,
+                          L, m, k, cand, idx, ws, ws_bytes, stream, ev);
 }
 
 int li_native_score(const void *keys, int key_t, const float *key_scale, const void *q, int q_t,

@@ -139,4 +139,10 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 // device), or nullptr on failure.
 int *device_status_ptr();
 
+// The argument checks of li_hs_select other than its workspace (LI_OK or the
+// error status), shared with the entry points that supply their own scratch.
+int hs_check_args(const void *latent, int lat_t, const float *lat_scale, const void *q_abs,
+                  int abs_t, const float *q_abs_scale, const float *w, const float *beta, int B,
+                  int G, int H, int r, int L, int m, int k, const int32_t *cand, const int32_t *idx);
+
 } // namespace li

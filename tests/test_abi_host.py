@@ -169,3 +169,26 @@ def test_append_argument_errors(L):
     assert call(lat_t=7) == LI_ERR_INVALID_ARG
     assert call(x=MIS) == LI_ERR_ALIGNMENT
     assert call(B=0) == LI_OK                         # nothing to do, no CUDA call
+
+
+def test_hs_profiled_needs_its_events(L):
+    ws = L.li_hs_workspace_size(2, 4, 1000, 256, 64)
+    assert L.li_hs_select_profiled(A, FP8, A, A, FP8, A, A, None, 2, 4, 64, 192, 1000, 256, 64,
+                                   A, A, A, ws, None, None) == LI_ERR_INVALID_ARG
+
+
+def test_hs_noalloc_reports_argument_errors_like_hs_select(L):
+    """The no-allocation entry point runs li_hs_select's argument checks before
+    its scratch-size limit: a call that is both malformed and too large gets
+    the argument error, as li_hs_select would give it."""
+    f = L.li_hs_select_noalloc
+    big = [A, FP8, A, A, FP8, A, A, None, 64, 4, 64, 192, 131072, 8192, 2048, A, A, None]
+    assert f(*big) == LI_ERR_WORKSPACE                          # valid, but more than 8 MiB of scratch
+    mis = list(big); mis[0] = MIS
+    assert f(*mis) == LI_ERR_ALIGNMENT
+    bad_t = list(big); bad_t[1] = 9
+    assert f(*bad_t) == LI_ERR_INVALID_ARG
+    no_scale = list(big); no_scale[2] = None                    # fp8 latent without its scales
+    assert f(*no_scale) == LI_ERR_INVALID_ARG
+    bad_mk = list(big); bad_mk[13] = 1024                       # m < k
+    assert f(*bad_mk) == LI_ERR_INVALID_ARG

@@ -333,6 +333,27 @@ def test_hs_matches_oracle(li, orc, dt):
     _hs_check(li, orc, x, 512, 128, dt)
 
 
+def test_hs_profiled_equals_hs_and_times_its_stages(li, orc):
+    """li_hs_select_profiled does the same work as li_hs_select (identical
+    candidates and selections, both checked against the oracle) and records
+    its six events in stream order."""
+    w = li_inputs.spec("fp8_128k_hs", B=2, L=40000, m=1024, k=256)
+    x = li_inputs.make_workload(w, seed=13)
+    c, gi, _ = _hs_check(li, orc, x, 1024, 256, "fp8")
+    qa, qs = li.absorb_queries(_dev(x["q"]), _dev(x["D"]), "fp8")
+    cand = torch.empty(2, 1024, dtype=torch.int32, device=DEV)
+    idx = torch.empty(2, 4, 256, dtype=torch.int32, device=DEV)
+    ws = torch.empty(li.li_hs_workspace_size(2, 4, 40000, 1024, 256), dtype=torch.uint8, device=DEV)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+    assert li.li_hs_select_profiled(_dev(x["latent"]), _dev(x["lat_scale"]), qa, qs, _dev(x["w"]),
+                                    1024, 256, cand, idx, ws, ev) == 0
+    _sync_ok(li)
+    np.testing.assert_array_equal(np.sort(cand.cpu().numpy(), axis=-1), np.sort(c, axis=-1))
+    np.testing.assert_array_equal(np.sort(idx.cpu().numpy(), axis=-1), np.sort(gi, axis=-1))
+    stages = [ev[i].elapsed_time(ev[i + 1]) for i in range(5)]
+    assert all(t >= 0 for t in stages) and sum(stages) > 0
+
+
 def test_hs_eight_layer_group(li, orc):
     """G = 8 at H = 64: the group scan and the followers' rescoring exceed one
     tensor-core tile (256 columns) and run in chunks of four layers."""
