@@ -57,6 +57,7 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-side", action="store_true", help="skip the HS / native side timings")
+    ap.add_argument("--no-configs", action="store_true", help="skip the per-config records")
     ap.add_argument("--cpu-sample-seconds", type=float, default=12.0)
     return ap.parse_args()
 
@@ -149,19 +150,18 @@ SCAN_SOURCES = ["shared_latent_key_cache_b300/csrc/score_tc.cu", "shared_latent_
 
 
 def ncu_traffic(workload: str):
-    """DRAM bytes (read + write) per launch of the scan kernel from the
-    committed ncu summary of this workload, if that capture was taken on the
-    current kernel sources (else None)."""
-    import re
-    p = os.path.join(ROOT, "profiles", f"decode_{workload}_kernels_full.md")
+    """DRAM bytes (read + write) per launch of the scan kernel for this
+    workload, from profiles/scan_dram_traffic.json (written from an ncu
+    capture), if that capture was taken on the current kernel sources; else
+    None."""
+    p = os.path.join(ROOT, "profiles", "scan_dram_traffic.json")
     if not os.path.exists(p):
         return None
-    text = open(p).read()
-    mh = re.search(r"scan_kernel_sources_sha256_16: ([0-9a-f]{16})", text)
-    mb = re.search(r"dram_bytes_per_launch: ([0-9]+)", text)
-    if not mh or not mb or mh.group(1) != source_hash(SCAN_SOURCES):
+    with open(p) as f:
+        rec = json.load(f).get(workload)
+    if not rec or rec.get("kernel_sources_sha256_16") != source_hash(SCAN_SOURCES):
         return None
-    return int(mb.group(1))
+    return int(rec["dram_bytes_per_launch"])
 
 
 class L2Flush:
@@ -233,10 +233,22 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ reference
 
-def cpu_oracle_rate(w, seed: int, budget_s: float):
-    """Time the fp64 CPU oracle (absorb + score + TopK) on whole sequences of the
-    workload until about `budget_s` seconds of work; returns the line's fields."""
-    import numpy as np  # noqa: F401
+CPU_SAMPLE = {  # name -> (unit of work timed on the host, how many at most)
+    "tiny_f32": ("sequence", 1),
+    "dsa_bf16_8k": ("sequence", 1),
+    "fp8_32k_b32": ("sequence", 32),
+    "fp8_128k_hs": ("sequence", 3),
+    "prefill_bf16_128k": ("query", 6),
+}
+
+
+def cpu_oracle_rate(w, seed: int, budget_s: float, max_units: int | None = None):
+    """Time the fp64 CPU oracle (absorb + score + TopK) on whole sequences of a
+    decode workload, or on single query positions of a prefill workload, until
+    about `budget_s` seconds of work or `max_units` units; returns the
+    record's fields, the full step's time extrapolated from the sample when
+    the sample is smaller than the step."""
+    import numpy as np
     import torch
 
     import li_inputs
@@ -244,14 +256,22 @@ def cpu_oracle_rate(w, seed: int, budget_s: float):
 
     oracle.build()
     cores = oracle.default_threads()
-    per_seq = step_bytes(li_inputs.spec(w.name, B=1))["total"]
-    T_sample = w.T if w.T == 1 else 1
-    done, elapsed, seqs = 0, 0.0, 0
-    bytes_done = 0
-    while (seqs == 0 or elapsed < budget_s) and seqs < w.B:
-        one = li_inputs.spec(w.name, B=1, T=T_sample, native=False,
-                             pos0=(w.pos0 + w.T - 1) if w.pos0 >= 0 else -1)
-        x = li_inputs.make_workload(one, seed=seed + 1000 + seqs)
+    unit, cap = CPU_SAMPLE.get(w.name, ("sequence", w.B))
+    cap = cap if max_units is None else max_units
+    total_units = w.B if unit == "sequence" else w.B * w.T
+    cap = min(cap, total_units)
+    elapsed, n = 0.0, 0
+    qpos_all = None
+    if unit == "query":
+        # evenly spread query positions, first and last included
+        qpos_all = [w.pos0 + round(i * (w.T - 1) / max(1, cap - 1)) for i in range(cap)]
+    while n < cap and (n == 0 or elapsed < budget_s):
+        if unit == "sequence":
+            one = li_inputs.spec(w.name, B=1, native=False)
+            x = li_inputs.make_workload(one, seed=seed + 1000 + n)
+        else:
+            one = li_inputs.spec(w.name, B=1, T=1, native=False, pos0=qpos_all[n])
+            x = li_inputs.make_workload(one, seed=seed + 1000)
         t0 = time.perf_counter()
         qabs = oracle.absorb(x["q"], x["D"])
         u = oracle.score(x["latent"], x["lat_scale"], qabs, x["w"], q_pos=x["q_pos"])
@@ -260,16 +280,20 @@ def cpu_oracle_rate(w, seed: int, budget_s: float):
             vl = np.full(one.G, int(x["q_pos"][0]) + 1, dtype=np.int32)
         oracle.topk(u.reshape(-1, one.L), one.k, valid_len=vl)
         elapsed += time.perf_counter() - t0
-        seqs += 1
-        bytes_done += step_bytes(one)["total"]
+        n += 1
         del x, qabs, u
-        torch.cuda.empty_cache() if torch.cuda.is_available() else None
-    gbs = bytes_done / elapsed / 1e9
-    sample = (f"{seqs} of {w.B} sequences of {w.name}" if w.T == 1 else
-              f"{seqs} query (last position) of {w.T} of {w.name}")
-    return {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
-            "sample": sample + f", fp64, {elapsed:.1f} s", "seconds": elapsed,
-            "bytes": bytes_done, "per_sequence_bytes": per_seq}
+    step_s = elapsed / n * total_units
+    gbs = step_bytes(w)["total"] / step_s / 1e9
+    extrap = n < total_units
+    what = (f"{n} of {w.B} sequences of {w.name}" if unit == "sequence" else
+            f"{n} of {w.T} query positions of {w.name} (spread over {w.pos0}..{w.pos0 + w.T - 1})")
+    sample = what + f", fp64, {elapsed:.1f} s" + (", full step extrapolated from the sample" if extrap else "")
+    rec = {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample,
+           "step_ms": step_s * 1e3, "extrapolated": extrap, "seconds": elapsed}
+    if w.T > 1:
+        q_pos = list(range(w.pos0, w.pos0 + w.T))
+        rec["tflops"] = scan_flops(w, q_pos) / step_s / 1e12
+    return rec
 
 
 def run_reference(a, w):
@@ -281,8 +305,7 @@ def run_reference(a, w):
     for i in range(max(1, a.steps if a.steps <= 3 else 1)):
         steps.append(cpu_oracle_rate(w, a.seed + i, a.cpu_sample_seconds))
     cb = steps[-1]
-    sb = step_bytes(w)["total"]
-    ms = sb / (cb["value"] * 1e9) * 1e3
+    ms = cb["step_ms"]
     line = {
         "impl": "reference", "metric": METRIC, "value": cb["value"], "unit": "GB/s",
         "n_gpus": a.gpus, "steps": len(steps), "warmup": 0, "ms_per_step": ms,
@@ -298,146 +321,194 @@ def run_reference(a, w):
 
 # ------------------------------------------------------------------------ ours
 
-def run_ours(a, w):
-    import torch
+PER_CONFIG = ["tiny_f32", "dsa_bf16_8k", "fp8_32k_b32", "fp8_128k_hs", "prefill_bf16_128k"]
+NATIVE_SIDE = {"dsa_bf16_8k", "fp8_32k_b32", "fp8_128k_hs"}     # configs timed against 4 native scans
 
-    import li_inputs
-    import shared_latent_key_cache_b300 as li
 
-    ws, rank, local = dist_env()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    if ws > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
+def _chk(li, st, what):
+    if st != 0:
+        raise RuntimeError(f"{what}: {li.li_status_string(st)}")
 
-    x = li_inputs.make_workload(li_inputs.spec(w.name, native=not a.no_side and w.T == 1),
-                                seed=a.seed + rank, device=dev)
-    absd = {"f32": "f32", "bf16": "bf16", "fp8": "fp8"}[w.lat_dtype]
-    stream = torch.cuda.current_stream(dev)
-    B, T, G, H, r, L, k = w.B, w.T, w.G, w.H, w.r, w.L, w.k
 
-    q_abs = torch.empty(B, T, G, H, r, dtype={"f32": torch.float32, "bf16": torch.bfloat16,
-                                              "fp8": torch.uint8}[absd], device=dev)
-    q_scale = torch.empty(B, T, G, H, dtype=torch.float32, device=dev) if absd == "fp8" else None
-    scores = torch.empty(B, T, G, L, dtype=torch.float32, device=dev)
-    idx = torch.empty(B, T, G, k, dtype=torch.int32, device=dev)
-    vl = None
-    if x["q_pos"] is not None:
-        vl = (x["q_pos"] + 1).repeat_interleave(G).contiguous()
-    flush = L2Flush(dev)
-    # top-k workspace for the two-pass selection of rows longer than 32,768
-    tws_n = li.li_topk_workspace_size(B * T * G, L, k) if vl is None else 0
-    tws = torch.empty(tws_n, dtype=torch.uint8, device=dev) if tws_n > 0 else None
+class Step:
+    """Device buffers and the three launches of one step of a workload:
+    absorb (eq. 6), group score (eq. 8), per-layer top-k."""
 
-    def chk(st, what):
-        if st != 0:
-            raise RuntimeError(f"{what}: {li.li_status_string(st)}")
+    def __init__(self, li, w, x, dev):
+        import torch
+        self.li, self.w, self.x = li, w, x
+        B, T, G, H, r, L, k = w.B, w.T, w.G, w.H, w.r, w.L, w.k
+        self.absd = {"f32": "f32", "bf16": "bf16", "fp8": "fp8"}[w.lat_dtype]
+        self.q_abs = torch.empty(B, T, G, H, r, dtype={"f32": torch.float32, "bf16": torch.bfloat16,
+                                                       "fp8": torch.uint8}[self.absd], device=dev)
+        self.q_scale = torch.empty(B, T, G, H, dtype=torch.float32, device=dev) if self.absd == "fp8" else None
+        self.scores = torch.empty(B, T, G, L, dtype=torch.float32, device=dev)
+        self.idx = torch.empty(B, T, G, k, dtype=torch.int32, device=dev)
+        self.vl = None
+        if x["q_pos"] is not None:
+            self.vl = (x["q_pos"] + 1).repeat_interleave(G).repeat(B).contiguous()
+        n = li.li_topk_workspace_size(B * T * G, L, k)
+        self.tws = torch.empty(n, dtype=torch.uint8, device=dev) if n > 0 else None
+        self.launches = 4 if self.tws is not None else 3
 
-    def step(ev=None):
+    def __call__(self, stream, ev=None):
+        li, x = self.li, self.x
         if ev is not None:
             ev[0].record(stream)
-        chk(li.li_absorb_queries(x["q"], x["D"], q_abs, q_scale, stream), "absorb")
+        _chk(li, li.li_absorb_queries(x["q"], x["D"], self.q_abs, self.q_scale, stream), "absorb")
         if ev is not None:
             ev[1].record(stream)
-        chk(li.li_score_group(x["latent"], x["lat_scale"], q_abs, q_scale, x["w"], scores,
-                              q_pos=x["q_pos"], stream=stream), "score")
+        _chk(li, li.li_score_group(x["latent"], x["lat_scale"], self.q_abs, self.q_scale, x["w"],
+                                   self.scores, q_pos=x["q_pos"], stream=stream), "score")
         if ev is not None:
             ev[2].record(stream)
-        chk(li.li_topk(scores, k, idx, None, vl, tws, stream), "topk")
+        _chk(li, li.li_topk(self.scores, self.w.k, self.idx, None, self.vl, self.tws, stream), "topk")
         if ev is not None:
             ev[3].record(stream)
 
-    for _ in range(a.warmup):
-        flush()
-        step()
-    st = li.li_device_status(stream)
-    if st != 0:
-        raise RuntimeError(li.li_status_string(st))
 
-    K = a.steps
-    # Headline: events at the step boundaries only, so the kernels of a step
-    # keep their programmatic launch overlap (an event recorded between two
-    # kernels would serialise them).
-    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    barrier = (lambda: torch.distributed.barrier()) if ws > 1 else (lambda: None)
-    barrier()
+def time_steps(step, n, flush, stream, dev, clk=None):
+    """n steps, L2 evicted before each (outside the events); per-step device ms
+    between events at the step's boundaries only (no event between kernels,
+    which would end their programmatic launch overlap)."""
+    import torch
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    nsamp = max(1, min(8, n // 1000))
+    sample_at = {int((j + 0.5) * n / nsamp) for j in range(nsamp)} if clk is not None else set()
     torch.cuda.synchronize(dev)
-    clk = ClockSampler(local)
-    nsamp = max(1, min(8, K // 1000))
-    sample_at = {int((j + 0.5) * K / nsamp) for j in range(nsamp)}
     t_wall = time.perf_counter()
-    for i in range(K):
+    for i in range(n):
         flush()
         ev0[i].record(stream)
-        step()
+        step(stream)
         ev1[i].record(stream)
         if i in sample_at:
             clk.sample()          # the GPU is still running the steps enqueued so far
     torch.cuda.synchronize(dev)
-    t_wall = time.perf_counter() - t_wall
-    barrier()
-    st = li.li_device_status(stream)
-    if st != 0:
-        raise RuntimeError(li.li_status_string(st))
-    step_ms = sum(ev0[i].elapsed_time(ev1[i]) for i in range(K))
-    ms_per_step = max_over_ranks(step_ms, ws, dev) / K
-    sb = step_bytes(w)
-    value = whole_job_rate(sb["total"], ws, ms_per_step)
+    return [ev0[i].elapsed_time(ev1[i]) for i in range(n)], time.perf_counter() - t_wall
 
-    # Per-kernel breakdown (and the scan's duration for the roofline): a second
-    # timed run of the same steps with an event between the kernels.
-    KB = min(K, 400)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(KB)]
-    for i in range(KB):
+
+def breakdown(step, n, flush, stream, dev):
+    """Median device us of absorb / score / top-k over n steps with events
+    between the kernels."""
+    import torch
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n)]
+    for i in range(n):
         flush()
-        step(evs[i])
+        step(stream, evs[i])
     torch.cuda.synchronize(dev)
-    st = li.li_device_status(stream)
-    if st != 0:
-        raise RuntimeError(li.li_status_string(st))
-    per = [[e[j].elapsed_time(e[j + 1]) for j in range(3)] for e in evs]
-    absorb_us = statistics.median(p[0] for p in per) * 1e3
-    score_us = statistics.mean(p[1] for p in per) * 1e3
-    topk_us = statistics.median(p[2] for p in per) * 1e3
-    clocks = clk.summary()
+    per = [[e[j].elapsed_time(e[j + 1]) * 1e3 for j in range(3)] for e in evs]
+    return {name: statistics.median(p[j] for p in per) for j, name in enumerate(("absorb", "score", "topk"))}
 
-    # ---- e2e: the same step through the C ABI with host buffers.  Every step
-    # copies its queries and head weights from pinned host memory and reads
-    # its selections back.  Steps alternate between two streams with their own
-    # device buffers, so one step's copies overlap another's kernels, as a
-    # serving loop would run them; the time is the whole run's, from one event
-    # before the first copy to the end of the last read-back.  No L2 flush
-    # here: every step streams the whole latent cache (more than the L2).
+
+def scored_positions(w, q_pos=None) -> int:
+    """Positions scored per step, summed over (sequence, query, layer)."""
+    if q_pos is not None:
+        return w.B * w.G * sum(min(int(t) + 1, w.L) for t in q_pos)
+    return w.B * w.T * w.G * w.L
+
+
+def roofline(w, score_us, q_pos, pk, kernel_note=""):
+    """The group scan's roofline: HBM for decode (algorithmic bytes per launch),
+    the tensor pipe for prefill-shaped scoring (flops of the causal pairs)."""
+    sbytes = scan_bytes(w)
+    sflops = scan_flops(w, q_pos)
+    if w.T > 1:
+        achieved = sflops / (score_us * 1e-6) / 1e12
+        peak = pk["bf16_tflops_sustained"] or pk["bf16_tflops"]
+        return {"kernel": "score_tc_kernel (causal prefill scoring)" + kernel_note, "bound": "tensor",
+                "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "traffic": ncu_traffic(w.name), "peak_source": pk["source"] + " cuBLAS bf16, sustained",
+                "algorithmic_bytes_per_launch": sbytes, "flops_per_launch": sflops}
+    achieved = sbytes / (score_us * 1e-6) / 1e9
+    kern = "score_simt_kernel (group scan, fp32)" if w.lat_dtype == "f32" else "score_tc_kernel (group scan)"
+    return {"kernel": kern + kernel_note, "bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"],
+            "unit": "GB/s", "frac": achieved / pk["hbm_gbs"], "traffic": ncu_traffic(w.name),
+            "peak_source": pk["source"] + " copy bandwidth",
+            "algorithmic_bytes_per_launch": sbytes, "flops_per_launch": sflops}
+
+
+def config_record(a, name, li, dev, stream, flush, cpu=True):
+    """One config's numbers: step latency, tokens scored per second, GB/s (and
+    TFLOP/s for prefill), the scan's roofline fraction, the oracle on the host
+    cores; HS and four native scans beside the 128K and 8K/32K decodes."""
+    import torch
+    import li_inputs
+    w = li_inputs.spec(name, native=(name in NATIVE_SIDE and not a.no_side))
+    x = li_inputs.make_workload(w, seed=a.seed, device=dev)
+    step = Step(li, w, x, dev)
+    n = {"tiny_f32": 200, "dsa_bf16_8k": 200, "fp8_32k_b32": 100, "fp8_128k_hs": 60,
+         "prefill_bf16_128k": 4}[name]
+    n = max(n, min(a.steps, 1000)) if w.T == 1 else n
+    for _ in range(max(3, min(a.warmup, 20)) if w.T == 1 else 2):
+        flush()
+        step(stream)
+    _chk(li, li.li_device_status(stream), name)
+    ts, _ = time_steps(step, n, flush, stream, dev)
+    _chk(li, li.li_device_status(stream), name)
+    lat_us = statistics.median(ts) * 1e3
+    kb = breakdown(step, min(n, 100), flush, stream, dev)
+    _chk(li, li.li_device_status(stream), name)
+    q_pos = x["q_pos"].tolist() if x["q_pos"] is not None else None
+    sb = step_bytes(w)
+    rec = {"workload": name, "B": w.B, "T": w.T, "L": w.L, "G": w.G, "H": w.H, "r": w.r, "k": w.k,
+           "latent": w.lat_dtype, "steps_timed": n, "latency_us": lat_us,
+           "tokens_scored_per_s": scored_positions(w, q_pos) / (lat_us * 1e-6),
+           "gbs": sb["total"] / (lat_us * 1e-6) / 1e9, "step_bytes": sb["total"],
+           "kernels_us": kb, "roofline": roofline(w, kb["score"], q_pos, peaks())}
+    if w.T > 1:
+        rec["tflops"] = scan_flops(w, q_pos) / (lat_us * 1e-6) / 1e12
+    if name == "tiny_f32" or name == "dsa_bf16_8k":
+        rec["note"] = "a few MB per step: launch-latency bound, not bandwidth bound"
+    if w.T == 1 and not a.no_side:
+        rec.update(side_timings(a, w, x, step, li, stream, flush, dev))
+    if cpu:
+        cb = cpu_oracle_rate(w, a.seed, a.cpu_sample_seconds)
+        rec["cpu_baseline"] = {k2: cb[k2] for k2 in ("value", "unit", "cores", "kind", "sample",
+                                                     "step_ms", "extrapolated")}
+        if "tflops" in cb:
+            rec["cpu_baseline"]["tflops"] = cb["tflops"]
+    del step, x
+    torch.cuda.empty_cache()
+    return rec
+
+
+def e2e_timing(a, w, x, step, li, dev, ws):
+    """The same step through the C ABI with host buffers: every step copies its
+    queries and head weights from pinned host memory and reads its selections
+    back.  Steps alternate between two streams with their own device buffers,
+    so one step's copies overlap another's kernels, as a serving loop would run
+    them; the time is the whole run's, from one event before the first copy to
+    the end of the last read-back.  No L2 flush here: every step streams the
+    whole latent cache (more than the L2).  Also times a bare pinned copy of
+    the same bytes each way on an idle GPU, the link's own bound."""
+    import torch
+    stream = torch.cuda.current_stream(dev)
     q_h = x["q"].cpu().pin_memory()
     w_h = x["w"].cpu().pin_memory()
     NS = 2
     streams = [torch.cuda.Stream(dev) for _ in range(NS)]
     slots = []
     for _ in range(NS):
-        slots.append({"q": torch.empty_like(x["q"]), "w": torch.empty_like(x["w"]),
-                      "q_abs": torch.empty_like(q_abs),
-                      "q_scale": torch.empty_like(q_scale) if q_scale is not None else None,
-                      "scores": torch.empty_like(scores), "idx": torch.empty_like(idx),
-                      "idx_h": torch.empty(idx.shape, dtype=torch.int32).pin_memory(),
-                      "tws": torch.empty_like(tws) if tws is not None else None})
+        sx = dict(x)
+        sx["q"], sx["w"] = torch.empty_like(x["q"]), torch.empty_like(x["w"])
+        st = Step(li, w, sx, dev)
+        slots.append({"step": st, "x": sx,
+                      "idx_h": torch.empty(st.idx.shape, dtype=torch.int32).pin_memory()})
 
     def e2e_step(i):
         st, sl = streams[i % NS], slots[i % NS]
         with torch.cuda.stream(st):
-            sl["q"].copy_(q_h, non_blocking=True)
-            sl["w"].copy_(w_h, non_blocking=True)
-            chk(li.li_absorb_queries(sl["q"], x["D"], sl["q_abs"], sl["q_scale"], st), "absorb")
-            chk(li.li_score_group(x["latent"], x["lat_scale"], sl["q_abs"], sl["q_scale"], sl["w"],
-                                  sl["scores"], q_pos=x["q_pos"], stream=st), "score")
-            chk(li.li_topk(sl["scores"], k, sl["idx"], None, vl, sl["tws"], st), "topk")
-            sl["idx_h"].copy_(sl["idx"], non_blocking=True)
+            sl["x"]["q"].copy_(q_h, non_blocking=True)
+            sl["x"]["w"].copy_(w_h, non_blocking=True)
+            sl["step"](st)
+            sl["idx_h"].copy_(sl["step"].idx, non_blocking=True)
 
     for i in range(2 * NS):                       # warm the streams
         e2e_step(i)
     torch.cuda.synchronize(dev)
-    E = min(K, 500)
+    E = min(a.steps, 500)
     ev_start = torch.cuda.Event(enable_timing=True)
     ev_end = torch.cuda.Event(enable_timing=True)
     ev_start.record(stream)
@@ -451,84 +522,141 @@ def run_ours(a, w):
         stream.wait_event(j)
     ev_end.record(stream)
     torch.cuda.synchronize(dev)
-    st_ = li.li_device_status(stream)
-    if st_ != 0:
-        raise RuntimeError(li.li_status_string(st_))
+    _chk(li, li.li_device_status(stream), "e2e")
     e2e_ms = max_over_ranks(ev_start.elapsed_time(ev_end) / E, ws, dev)
     h2d = q_h.numel() * q_h.element_size() + w_h.numel() * w_h.element_size()
     d2h = slots[0]["idx_h"].numel() * slots[0]["idx_h"].element_size()
 
-    # ---- side timings on the same batch: HS, and 4 native per-layer scans + top-k
-    side = {}
-    if not a.no_side and T == 1:
-        side = side_timings(a, w, x, q_abs, q_scale, li, stream, flush, dev)
+    # bare pinned copies of the same sizes, one direction at a time
+    def bare(fn, reps=50):
+        fn()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / reps
+    dq, dw = torch.empty_like(x["q"]), torch.empty_like(x["w"])
+    h2d_ms = bare(lambda: (dq.copy_(q_h, non_blocking=True), dw.copy_(w_h, non_blocking=True)))
+    d2h_ms = bare(lambda: slots[0]["idx_h"].copy_(slots[0]["step"].idx, non_blocking=True))
+    return {"ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "steps": E, "streams": NS,
+            "link": {"h2d_us": h2d_ms * 1e3, "h2d_gbs": h2d / (h2d_ms * 1e-3) / 1e9,
+                     "d2h_us": d2h_ms * 1e3, "d2h_gbs": d2h / (d2h_ms * 1e-3) / 1e9,
+                     "how": "the step's own copies alone on an idle GPU, pinned host memory, mean of 50"}}
 
-    # ---- roofline of the dominant kernel (the group scan)
-    pk = peaks()
-    sbytes = scan_bytes(w)
-    sflops = scan_flops(w, x["q_pos"].tolist() if x["q_pos"] is not None else None)
-    if T > 1:
-        # prefill-shaped scoring is a dense contraction: tensor-bound
-        achieved = sflops / (score_us * 1e-6) / 1e12
-        peak = pk["bf16_tflops_sustained"] or pk["bf16_tflops"]
-        roof = {"kernel": "score_tc_kernel (causal prefill scoring)", "bound": "tensor",
-                "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "traffic": None, "peak_source": pk["source"] + " cuBLAS bf16, sustained (a ~35 ms kernel)",
-                "algorithmic_bytes_per_launch": sbytes, "flops_per_launch": sflops}
-    else:
-        achieved = sbytes / (score_us * 1e-6) / 1e9
-        tr = ncu_traffic(w.name)
-        roof = {"kernel": "score_tc_kernel (group scan)", "bound": "hbm", "achieved": achieved,
-                "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
-                "traffic": tr, "peak_source": pk["source"] + " copy bandwidth",
-                "algorithmic_bytes_per_launch": sbytes, "flops_per_launch": sflops}
+
+def run_ours(a, w):
+    import torch
+
+    import li_inputs
+    import shared_latent_key_cache_b300 as li
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    x = li_inputs.make_workload(li_inputs.spec(w.name, native=False), seed=a.seed + rank, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = L2Flush(dev)
+    step = Step(li, w, x, dev)
+
+    for _ in range(a.warmup):
+        flush()
+        step(stream)
+    _chk(li, li.li_device_status(stream), "warm-up")
+
+    K = a.steps
+    barrier = (lambda: torch.distributed.barrier()) if ws > 1 else (lambda: None)
+    barrier()
+    clk = ClockSampler(local)
+    ts, t_wall = time_steps(step, K, flush, stream, dev, clk)
+    barrier()
+    _chk(li, li.li_device_status(stream), "timed steps")
+    ms_per_step = max_over_ranks(sum(ts), ws, dev) / K
+    sb = step_bytes(w)
+    value = whole_job_rate(sb["total"], ws, ms_per_step)
+    kb = breakdown(step, min(K, 400), flush, stream, dev)
+    clocks = clk.summary()
+    e2e = e2e_timing(a, w, x, step, li, dev, ws)
+    q_pos = x["q_pos"].tolist() if x["q_pos"] is not None else None
+    roof = roofline(w, kb["score"], q_pos, peaks())
+    launches = step.launches * K
+    del step, x
+    torch.cuda.empty_cache()
+
+    per_config = {}
+    if rank == 0 and ws == 1 and not a.no_configs:
+        for name in PER_CONFIG:
+            if name == w.name:
+                continue
+            per_config[name] = config_record(a, name, li, dev, stream, flush)
 
     if rank == 0:
         cb = None
         if ws == 1:
             cb = cpu_oracle_rate(w, a.seed, a.cpu_sample_seconds)
             cb = {k2: cb[k2] for k2 in ("value", "unit", "cores", "kind", "sample")}
+        main = {"workload": w.name, "latency_us": ms_per_step * 1e3,
+                "tokens_scored_per_s": scored_positions(w, q_pos) * ws / (ms_per_step * 1e-3),
+                "gbs": value, "kernels_us": kb, "roofline": roof, "cpu_baseline": cb,
+                "note": "this record is the contract line itself"}
+        if not a.no_side and w.T == 1:
+            sx = li_inputs.make_workload(li_inputs.spec(w.name, native=True), seed=a.seed, device=dev)
+            sstep = Step(li, w, sx, dev)
+            main.update(side_timings(a, w, sx, sstep, li, stream, flush, dev))
+            del sstep, sx
+            torch.cuda.empty_cache()
+        per_config = {w.name: main, **per_config}
+        per_config = {n: per_config[n] for n in PER_CONFIG if n in per_config}
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": K,
             "warmup": a.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": w.lat_dtype, "data": "synthetic",
-            "config": {"workload": w.name, "B": B, "T": T, "L": L, "G": G, "H": H, "d": w.d, "r": r,
-                       "k": k, "latent": {"fp8": "fp8 e4m3 + fp32 per-token scale", "bf16": "bf16",
-                                          "f32": "fp32"}[w.lat_dtype],
+            "config": {"workload": w.name, "B": w.B, "T": w.T, "L": w.L, "G": w.G, "H": w.H, "d": w.d,
+                       "r": w.r, "k": w.k, "latent": {"fp8": "fp8 e4m3 + fp32 per-token scale",
+                                                      "bf16": "bf16", "f32": "fp32"}[w.lat_dtype],
                        "step": "absorb + 4-layer group score + per-layer top-k",
                        "l2": "evicted before every step by reading a 256 MiB buffer (no dirty lines left), outside the timed events; inputs also exceed L2",
                        "parallelism": f"replicas{ws}" if ws > 1 else "single GPU"},
             "latency_us": ms_per_step * 1e3,
-            "tokens_scored_per_s": B * T * G * L * ws / (ms_per_step * 1e-3),
-            "kernels_us": {"absorb": absorb_us, "score": score_us, "topk": topk_us},
-            "kernels_timing": f"{KB} further steps with an event between the kernels (those events "
-                              "stop the launch overlap, so the three sum to more than latency_us)",
+            "tokens_scored_per_s": main["tokens_scored_per_s"],
+            "kernels_us": kb,
+            "kernels_timing": f"medians of {min(K, 400)} further steps with an event between the kernels "
+                              "(those events stop the launch overlap, so the three sum to more than latency_us)",
             "step_bytes": sb,
             "wall_s_timed": t_wall,
-            "e2e": {"value": whole_job_rate(sb["total"], ws, e2e_ms), "unit": "GB/s",
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                    "steps": E, "streams": NS,
+            "e2e": {"value": whole_job_rate(sb["total"], ws, e2e["ms_per_step"]), "unit": "GB/s",
+                    **e2e,
                     "timing": "whole run of E steps between two events; steps alternate between two "
                               "streams so copies overlap kernels; no L2 flush (each step streams the "
                               "whole latent cache)",
                     "resident": "latent cache and decoders (device state across decode steps)"},
-            "gpu_launches": (4 if tws is not None else 3) * K,   # absorb, scan, top-k (two passes for long rows)
+            "gpu_launches": launches,
             "roofline": roof,
             "clocks": clocks,
             "cpu_baseline": cb,
+            "per_config": per_config,
         }
-        line.update(side)
         print(json.dumps(line), flush=True)
     if ws > 1:
         torch.distributed.destroy_process_group()
 
 
-def side_timings(a, w, x, q_abs, q_scale, li, stream, flush, dev):
+def side_timings(a, w, x, step, li, stream, flush, dev):
+    """Beside a decode config: the latent append of one new token per sequence,
+    hierarchical selection (total and per launch), and four native per-layer
+    DSA scans with (and without) their top-k, on the same batch."""
     import torch
     import li_inputs
     B, G, H, r, L, k, d = w.B, w.G, w.H, w.r, w.L, w.k, w.d
     out = {}
-    reps = max(5, min(200, a.steps // 10))
+    reps = max(5, min(200, a.steps // 10, 60 if L > 65536 else 200))
 
     def timeit(fn):
         for _ in range(3):
@@ -562,6 +690,7 @@ def side_timings(a, w, x, q_abs, q_scale, li, stream, flush, dev):
                      "bytes": ap_bytes, "gbs": ap_bytes / (ap_us * 1e-6) / 1e9}
 
     m = w.m if w.m else 8192
+    q_abs, q_scale = step.q_abs, step.q_scale
     if m <= L:
         cand = torch.empty(B, m, dtype=torch.int32, device=dev)
         hidx = torch.empty(B, G, k, dtype=torch.int32, device=dev)
@@ -573,8 +702,25 @@ def side_timings(a, w, x, q_abs, q_scale, li, stream, flush, dev):
                                   hidx, wsb, None, stream)
             assert st == 0
         hs_us = timeit(hs)
-        out["hs"] = {"m": m, "latency_us": hs_us,
-                     "scored_positions_per_seq": L + (G - 1) * min(m, L)}
+        # per launch: absorb first, then the five launches of the selection between events
+        stages = []
+        for i in range(reps):
+            flush()
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(7)]
+            ev[0].record(stream)
+            assert li.li_absorb_queries(x["q"], x["D"], q_abs, q_scale, stream) == 0
+            assert li.li_hs_select_profiled(x["latent"], x["lat_scale"], q_abs, q_scale, x["w"], m, k,
+                                            cand, hidx, wsb, ev[1:], None, stream) == 0
+            stages.append(ev)
+        torch.cuda.synchronize(dev)
+        names = ["absorb", "anchor_scan", "anchor_top_m", "anchor_top_k", "follower_rescore",
+                 "follower_top_k"]
+        per = {nm: statistics.median(e[j].elapsed_time(e[j + 1]) * 1e3 for e in stages)
+               for j, nm in enumerate(names)}
+        out["hs"] = {"m": m, "latency_us": hs_us, "stages_us": per,
+                     "stages_timing": "medians with an event between the launches",
+                     "scored_positions_per_seq": L + (G - 1) * min(m, L),
+                     "tokens_scored_per_s": B * (L + (G - 1) * min(m, L)) / (hs_us * 1e-6)}
 
     if "keys" in x:
         q8 = torch.empty(B, 1, 1, H, d, dtype=torch.uint8, device=dev)

@@ -177,9 +177,14 @@ def li_hs_select(latent, lat_scale, q_abs, q_abs_scale, w, m: int, k: int, cand,
 
 def li_hs_select_profiled(latent, lat_scale, q_abs, q_abs_scale, w, m: int, k: int, cand, idx, ws,
                           events, beta=None, stream=None) -> int:
-    """li_hs_select with six torch.cuda.Event objects recorded around its five launches."""
+    """li_hs_select with six torch.cuda.Event objects recorded around its five launches.
+    torch creates an event's CUDA handle on its first record, so each event is
+    recorded once here (on the same stream) before the library records it again."""
     B, L, r = latent.shape
     _, _, G, H, _ = q_abs.shape
+    st = stream if stream is not None else torch.cuda.current_stream()
+    for e in events:
+        e.record(st)
     arr = (ctypes.c_void_p * 6)(*[ctypes.c_void_p(e.cuda_event) for e in events])
     return _lib.li_hs_select_profiled(
         _ptr(latent), _dtype_code(latent), _ptr(lat_scale), _ptr(q_abs), _dtype_code(q_abs),
@@ -260,7 +265,7 @@ def topk(scores, k: int, valid_len=None, with_vals: bool = False, out=None, ws=N
     shape = scores.shape[:-1] + (k,)
     idx = out if out is not None else torch.empty(shape, dtype=torch.int32, device=scores.device)
     vals = torch.empty(shape, dtype=torch.float32, device=scores.device) if with_vals else None
-    if ws is None and valid_len is None and scores.shape[-1] > 0:
+    if ws is None and scores.shape[-1] > 0:
         n = li_topk_workspace_size(scores.numel() // scores.shape[-1], scores.shape[-1], k)
         if n > 0:
             ws = torch.empty(n, dtype=torch.uint8, device=scores.device)

@@ -22,22 +22,29 @@
 //   warp 0          TMEM allocation; MMA issuer of the CTA's even tiles
 //   warp after the producers: MMA issuer of the odd tiles (two issuers keep
 //                   one tile's MMAs queued while the other's execute)
-//   warp 1          scan mode: TMA producer of the latent tiles (smem ring) and
-//                   of the absorbed-query operand (double-buffered when it
-//                   fits, so the next query's operand loads under the current
-//                   query's tiles)
+//   warp 1          scan mode: TMA producer of the latent tiles (smem ring),
+//                   of each tile's 128 fp32 token scales (fp8 latents; into
+//                   the same stage, on the same barrier) and of the absorbed-query
+//                   operand (double-buffered when it fits, so the next
+//                   query's operand loads under the current query's tiles)
 //   warps 1-2       gather mode (HS followers rescoring the anchor's
 //                   candidates): each thread copies two tile rows of gathered
 //                   latent with 16-byte cp.async into the swizzled layout TMA
 //                   would write, several tiles in flight per thread
-//   8 warps         epilogue, two per TMEM lane quarter (warp % 4), each
-//                   owning 128 accumulator columns (two layers at H = 64): two
-//                   64-column TMEM loads in flight, the accumulator released
-//                   as soon as they land, then ReLU, weighted head sums with
-//                   packed fp32 FMA, per-token scale (prefetched one tile
-//                   ahead) and one coalesced store per layer.  (Sixteen warps
-//                   of 64 columns, or two groups of eight taking alternate
-//                   tiles, measured the same time.)
+//   16 warps        epilogue (8 at H = 128), four per TMEM lane quarter
+//                   (warp % 4), each owning 64 accumulator columns (one layer
+//                   at H = 64; 128 columns at H = 128): its columns in flight
+//                   at once, the accumulator released as soon as they land,
+//                   then ReLU, weighted head sums with packed fp32 FMA, the
+//                   token's scale (read from the stage, which is then handed
+//                   back) and one coalesced store per layer.
+// The epilogue sets the tile period: each warp's chain per tile is wait,
+// accumulator load, arithmetic, store.  Measured with per-role clock stamps
+// (32 sequences x 32K, fp8): the MMAs of the next tile are complete before
+// the epilogue has released the current one.  Two changes shortened that
+// chain: the token scales arrive with the tile (a global load issued one tile
+// ahead cost a full HBM round trip per tile), and 64 instead of 128 columns
+// per warp halve its arithmetic.
 // The two TMEM accumulators (2 x 256 columns) are double-buffered so the
 // epilogue of tile i overlaps the MMAs of tile i+1 and the loads of the tiles
 // after it.
@@ -49,6 +56,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <cstring>
 #include <mutex>
 
 #include "li_internal.cuh"
@@ -60,19 +68,28 @@ namespace {
 constexpr int kTileM = 128;
 constexpr int kChunkElems = 64;
 constexpr int kMaxDev = 64;
-constexpr int kEpiWarps = 8;
 constexpr int kTmemCols = 512;          // two accumulators of 256 columns
 constexpr int kAccStride = 256;
 constexpr int kConstCap = 1024;         // active epilogue warps x columns per warp
 constexpr int kSmemLimit = 227 * 1024;
 
-template <bool kGather>
+// Epilogue warps own 64 accumulator columns each (one layer at H = 64), four
+// per 64-column block (one per TMEM lane quarter); at H = 128 a layer's
+// weighted sum spans 128 columns, so its warps own 128.
+template <int kH>
+struct EpiShape {
+    static constexpr int kCols = kH == 128 ? 128 : 64;
+    static constexpr int kWarps = 4 * (256 / kCols);
+};
+
+template <bool kGather, int kH>
 struct Roles {
     static constexpr int kMmaWarp = 0;                        // even tiles (accumulator 0)
     static constexpr int kProdWarp0 = 1;
     static constexpr int kProdWarps = kGather ? 2 : 1;
     static constexpr int kMmaWarp1 = kProdWarp0 + kProdWarps;  // odd tiles (accumulator 1)
     static constexpr int kEpiWarp0 = kMmaWarp1 + 1;
+    static constexpr int kEpiWarps = EpiShape<kH>::kWarps;
     static constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
 };
 
@@ -87,10 +104,12 @@ struct TcConfig {
     int b_bytes;        // one query operand
     int b_buf_stride;   // 1024-aligned
     int off_a;          // byte offsets from the 1024-aligned base
+    int off_sc;         // per-stage token scales (sc_stage)
     int off_bar;
     int off_misc;
     int cw;             // accumulator columns per epilogue warp
     int nepi;           // epilogue warps with columns
+    int sc_stage;       // the latent's per-token scales travel with each tile (TMA into the stage)
     int gdepth;         // gather mode: tiles in flight per copying thread
     int NT;             // tiles per query row
     int64_t U;          // total work units
@@ -201,11 +220,11 @@ __device__ __forceinline__ void cp_async_wait_depth(int depth)
 }
 
 template <bool kFP8, bool kGather, bool kBeta, int kH>
-__global__ void __launch_bounds__(Roles<kGather>::kThreads, 1)
+__global__ void __launch_bounds__(Roles<kGather, kH>::kThreads, 1)
     score_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    const ScoreParams p, const TcConfig c)
+                    const __grid_constant__ CUtensorMap tmS, const ScoreParams p, const TcConfig c)
 {
-    using R = Roles<kGather>;
+    using R = Roles<kGather, kH>;
     constexpr int kEsz = kFP8 ? 1 : 2;
     constexpr int kKStep = 32 / kEsz;              // elements per MMA K step (32 bytes)
     constexpr int kStepsPerChunk = kChunkElems / kKStep;
@@ -219,6 +238,7 @@ __global__ void __launch_bounds__(Roles<kGather>::kThreads, 1)
     uint8_t *base = smem_raw + (((raw_u32 + 1023u) & ~1023u) - raw_u32);
     uint8_t *smB = base;
     uint8_t *smA = base + c.off_a;
+    float *smS = reinterpret_cast<float *>(base + c.off_sc);   // [stages][128] token scales
     uint64_t *full = reinterpret_cast<uint64_t *>(base + c.off_bar);
     uint64_t *empty = full + c.stages;
     Bars *bars = reinterpret_cast<Bars *>(empty + c.stages);
@@ -234,7 +254,9 @@ __global__ void __launch_bounds__(Roles<kGather>::kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < c.stages; ++s) {
             mbar_init(&full[s], kGather ? static_cast<uint32_t>(R::kProdWarps) : 1u);
-            mbar_init(&empty[s], 1u);
+            // the MMAs' commit, and each epilogue warp once it has read the
+            // stage's token scales
+            mbar_init(&empty[s], 1u + static_cast<uint32_t>(c.sc_stage ? c.nepi : 0));
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&bars->b_full[a], 1u);
@@ -362,6 +384,8 @@ __global__ void __launch_bounds__(Roles<kGather>::kThreads, 1)
         if (lane == 0) {
             tma_prefetch_desc(&tmA);
             tma_prefetch_desc(&tmB);
+            if (c.sc_stage)
+                tma_prefetch_desc(&tmS);
         }
         const uint64_t pol = make_l2_policy(p.T == 1);   // decode: each tile is read once
         int stage = 0;
@@ -381,11 +405,15 @@ __global__ void __launch_bounds__(Roles<kGather>::kThreads, 1)
                 break;
             if (lane == 0) {
                 uint8_t *dstA = smA + stage * c.a_stage_bytes;
-                mbar_arrive_expect_tx(&full[stage], static_cast<uint32_t>(c.a_stage_bytes));
+                mbar_arrive_expect_tx(&full[stage], static_cast<uint32_t>(c.a_stage_bytes) +
+                                                        (c.sc_stage ? kTileM * 4u : 0u));
                 const int b = seq_of(w.bt, p.T);
                 for (int ch = 0; ch < c.nchunk; ++ch)
                     tma_load_3d_hint(dstA + ch * c.a_chunk_bytes, &tmA, &full[stage],
                                      ch * kChunkElems, w.tile * kTileM, b, pol);
+                // the tile's 128 token scales (zero past the cache end)
+                if (c.sc_stage)
+                    tma_load_2d(smS + stage * kTileM, &tmS, &full[stage], w.tile * kTileM, b);
             }
             __syncwarp();
             ++issued;
@@ -509,22 +537,24 @@ __global__ void __launch_bounds__(Roles<kGather>::kThreads, 1)
         __syncwarp();
     } else if (warp >= R::kEpiWarp0) {
         // ------------------------------------------------------------ epilogue
-        const int e = warp - R::kEpiWarp0;          // 0..7
+        constexpr int kCw = EpiShape<kH>::kCols;    // accumulator columns per warp
+        const int e = warp - R::kEpiWarp0;
         const int quarter = warp & 3;               // TMEM lane quarter
-        const int c0 = (e >> 2) * c.cw;             // first accumulator column
+        const int c0 = (e >> 2) * kCw;              // first accumulator column
         if (c0 < c.N) {
-            const int ncols = min(c.cw, c.N - c0);
+            const int ncols = min(kCw, c.N - c0);
             const int l0 = c0 / kH;                 // first layer (within the Gs scored)
             const int nlay = (ncols + kH - 1) / kH;
             const int row = quarter * 32 + lane;
-            float *wq = misc->wq + e * c.cw;
-            float *sq = misc->sq + e * c.cw;
-            float *bq = misc->bq + e * c.cw;
+            float *wq = misc->wq + e * kCw;
+            float *sq = misc->sq + e * kCw;
+            float *bq = misc->bq + e * kCw;
             const uint32_t tq = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                 static_cast<uint32_t>(c0);
-
-            // per-token scale: one tile ahead (scan), or index two tiles and
-            // scale one tile ahead (gather)
+            // Per-token latent scale: in scan mode it arrived with the tile in
+            // the stage's scale slot; gathering (HS followers) loads the
+            // gathered token's scale one tile ahead, its index two tiles ahead.
+            const bool stage_sc = !kGather && c.sc_stage;
             auto tok_of = [&](const Walk<kGather> &x) -> int {
                 const int pos = x.tile * kTileM + row;
                 if (!x.ok() || pos >= x.Lv)
@@ -543,7 +573,7 @@ __global__ void __launch_bounds__(Roles<kGather>::kThreads, 1)
 
             Walk<kGather> w;
             w.init(p, u_begin, u_end, c.NT);
-            float sc_cur = scale_of(w, tok_of(w));
+            float sc_cur = stage_sc ? 0.f : scale_of(w, tok_of(w));
             float sc_next = 0.f;
             int tok1 = 0;                           // gather: token of the next unit
             if (kGather) {
@@ -553,10 +583,12 @@ __global__ void __launch_bounds__(Roles<kGather>::kThreads, 1)
             }
             int acc = 0;
             uint32_t acc_phase = 0;
+            int est = 0;                            // the tile's stage (stage_sc)
+            uint32_t est_phase = 0;
             int cur_bt = -1;
             while (w.ok()) {
                 int tok2 = 0;
-                {
+                if (!stage_sc) {
                     // look ahead: the next unit's scale (its gathered index was
                     // loaded a tile ago) and, when gathering, the index after it
                     Walk<kGather> t = w;
@@ -579,7 +611,7 @@ __global__ void __launch_bounds__(Roles<kGather>::kThreads, 1)
                             bq[j] = p.beta[wrow + j];
                         } else {
                             // columns 2 and 3 of every 4 take the ReLU as (x + |x|) / 2
-                            // on the FMA pipe (see the epilogue): their weight is halved
+                            // on the FMA pipe (see below): their weight is halved
                             wq[j] = (j & 3) >= 2 ? 0.5f * (wv * sv) : wv * sv;
                         }
                     }
@@ -591,7 +623,21 @@ __global__ void __launch_bounds__(Roles<kGather>::kThreads, 1)
                 tc_fence_after();
                 const int pos = w.tile * kTileM + row;
                 const bool valid = pos < w.Lv;
-                const float sc = sc_cur;
+                float sc = sc_cur;
+                if (stage_sc) {
+                    // the stage's copies have landed (their barrier completed before
+                    // the MMAs ran); read this token's scale, then give the stage back
+                    if (!warp_wait(&full[est], est_phase, abort_flag, p.status))
+                        break;
+                    sc = smS[est * kTileM + row];
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(&empty[est]);
+                    if (++est == c.stages) {
+                        est = 0;
+                        est_phase ^= 1u;
+                    }
+                }
                 float *out = p.scores + (w.bt * (p.Gout ? p.Gout : Gs) + p.gout0 + l0) *
                                             static_cast<int64_t>(p.L_out) + pos;
                 const uint32_t tacc = tq + static_cast<uint32_t>(acc * kAccStride);
@@ -647,47 +693,52 @@ __global__ void __launch_bounds__(Roles<kGather>::kThreads, 1)
                         y = x;
                     }
                 };
-                // All of the warp's (<= 128) columns in flight at once; the
-                // accumulator is released as soon as they have landed.
-                uint32_t va[32], vb[32], vc[32], vd[32];
-                // 64-column loads where possible: half the load instructions of
-                // 32-column ones (measured 3 % off the scan)
+                // All of the warp's columns in flight at once; the accumulator is
+                // released as soon as they have landed.
+                uint32_t va[32], vb[32];
                 if (ncols > 32)
                     tmem_ld64(tacc, va, vb);
                 else
                     tmem_ld32(tacc, va);
-                if (ncols > 96)
-                    tmem_ld64(tacc + 64u, vc, vd);
-                else if (ncols > 64)
-                    tmem_ld32(tacc + 64u, vc);
-                tmem_ld_wait32(va);
-                tmem_regs_ready(vb);
-                tmem_regs_ready(vc);
-                tmem_regs_ready(vd);
-                // A relaxed arrival: a release would first wait for this warp's
-                // outstanding global loads and stores (the next tile's scale
-                // prefetch, the last tile's scores).
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive_relaxed(&bars->tmem_empty[acc]);
-                float2 x0 = make_float2(0.f, 0.f), y0 = x0, x1 = x0, y1 = x0;
-                chunk(va, 0, x0, y0);
-                if (ncols > 32)
-                    chunk(vb, 32, x0, y0);
-                if (kH == 64) {
-                    finish(0, (x0.x + x0.y) + (y0.x + y0.y));
-                    x0 = make_float2(0.f, 0.f);
-                    y0 = x0;
-                }
-                if (ncols > 64)
-                    chunk(vc, 64, x1, y1);
-                if (ncols > 96)
-                    chunk(vd, 96, x1, y1);
-                if (kH == 64 && ncols > 64)
-                    finish(1, (x1.x + x1.y) + (y1.x + y1.y));
-                if (kH == 128)
+                if constexpr (kCw > 64) {
+                    uint32_t vc[32], vd[32];
+                    if (ncols > 96)
+                        tmem_ld64(tacc + 64u, vc, vd);
+                    else if (ncols > 64)
+                        tmem_ld32(tacc + 64u, vc);
+                    tmem_ld_wait32(va);
+                    tmem_regs_ready(vb);
+                    tmem_regs_ready(vc);
+                    tmem_regs_ready(vd);
+                    // A relaxed arrival: a release would first wait for this warp's
+                    // outstanding global loads and stores.
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive_relaxed(&bars->tmem_empty[acc]);
+                    float2 x0 = make_float2(0.f, 0.f), y0 = x0, x1 = x0, y1 = x0;
+                    chunk(va, 0, x0, y0);
+                    if (ncols > 32)
+                        chunk(vb, 32, x0, y0);
+                    if (ncols > 64)
+                        chunk(vc, 64, x1, y1);
+                    if (ncols > 96)
+                        chunk(vd, 96, x1, y1);
                     finish(0, ((x0.x + x0.y) + (y0.x + y0.y)) + ((x1.x + x1.y) + (y1.x + y1.y)));
+                } else {
+                    tmem_ld_wait32(va);
+                    tmem_regs_ready(vb);
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive_relaxed(&bars->tmem_empty[acc]);
+                    float2 x0 = make_float2(0.f, 0.f), y0 = x0;
+                    chunk(va, 0, x0, y0);
+                    if (ncols > 32)
+                        chunk(vb, 32, x0, y0);
+                    if (kH == 64)
+                        finish(0, (x0.x + x0.y) + (y0.x + y0.y));
+                }
                 w.next(p, c.NT);
                 sc_cur = sc_next;
                 tok1 = tok2;
@@ -707,6 +758,14 @@ __global__ void __launch_bounds__(Roles<kGather>::kThreads, 1)
 
 // ------------------------------------------------------------------ host side
 
+// The latent's per-token fp32 scales are copied into each stage next to the
+// tile (one 512-byte TMA box) in scan mode when the scale rows can be a TMA
+// tensor: row stride L * 4 a multiple of 16 bytes.
+bool scales_in_stage(const ScoreParams &p)
+{
+    return p.gather_idx == nullptr && p.lat_scale != nullptr && p.L_lat % 4 == 0;
+}
+
 bool make_config(const ScoreParams &p, bool fp8, TcConfig &c, int &smem_bytes)
 {
     const int esz = fp8 ? 1 : 2;
@@ -717,15 +776,17 @@ bool make_config(const ScoreParams &p, bool fp8, TcConfig &c, int &smem_bytes)
     c.a_stage_bytes = c.nchunk * c.a_chunk_bytes;
     c.b_bytes = c.nchunk * c.b_chunk_bytes;
     c.b_buf_stride = (c.b_bytes + 1023) & ~1023;
+    c.sc_stage = scales_in_stage(p) ? 1 : 0;
+    const int sc_bytes = c.sc_stage ? kTileM * 4 : 0;      // per stage
     const int bar_bytes = 2 * 8 * 8 + static_cast<int>(sizeof(Bars));
     const int fixed = 1024 /* alignment slack */ + ((bar_bytes + 15) & ~15) +
                       static_cast<int>(sizeof(Misc));
     // Two query-operand buffers when that still leaves >= 3 latent stages.
-    int stages = (kSmemLimit - fixed - 2 * c.b_buf_stride) / c.a_stage_bytes;
+    int stages = (kSmemLimit - fixed - 2 * c.b_buf_stride) / (c.a_stage_bytes + sc_bytes);
     c.nbuf = 2;
     if (stages < 3) {
         c.nbuf = 1;
-        stages = (kSmemLimit - fixed - c.b_buf_stride) / c.a_stage_bytes;
+        stages = (kSmemLimit - fixed - c.b_buf_stride) / (c.a_stage_bytes + sc_bytes);
     }
     if (stages > 8)
         stages = 8;
@@ -733,24 +794,25 @@ bool make_config(const ScoreParams &p, bool fp8, TcConfig &c, int &smem_bytes)
         return false;
     c.stages = stages;
     c.off_a = c.nbuf * c.b_buf_stride;
-    c.off_bar = c.off_a + stages * c.a_stage_bytes;
+    c.off_sc = c.off_a + stages * c.a_stage_bytes;
+    c.off_bar = c.off_sc + stages * sc_bytes;
     c.off_misc = (c.off_bar + 2 * stages * 8 + static_cast<int>(sizeof(Bars)) + 15) & ~15;
     smem_bytes = c.off_misc + static_cast<int>(sizeof(Misc)) + 1024;
     // one CTA per SM: a second CTA would only queue on the TMEM allocation
     if (smem_bytes < 116 * 1024)
         smem_bytes = 116 * 1024;
-    c.cw = 128;                           // accumulator columns per epilogue warp
+    c.cw = p.H == 128 ? 128 : 64;         // accumulator columns per epilogue warp (EpiShape)
     c.nepi = 4 * ((c.N + c.cw - 1) / c.cw);
     c.gdepth = stages - 1 < 3 ? stages - 1 : 3;
     const int Lrow = p.gather_idx ? p.L_out : p.L_lat;
     c.NT = (Lrow + kTileM - 1) / kTileM;
     c.U = static_cast<int64_t>(p.B) * p.T * c.NT;
-    return smem_bytes <= kSmemLimit && c.nepi <= kEpiWarps && c.nepi * c.cw <= kConstCap &&
-           c.cw <= 128;
+    return smem_bytes <= kSmemLimit && c.nepi <= 4 * (256 / c.cw) && c.nepi * c.cw <= kConstCap;
 }
 
 template <bool kFP8, bool kGather, bool kBeta, int kH>
-cudaError_t launch_t(const CUtensorMap &tmA, const CUtensorMap &tmB, const ScoreParams &p,
+cudaError_t launch_t(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmS,
+                     const ScoreParams &p,
                      const TcConfig &c, int smem_bytes, cudaStream_t s)
 {
     auto kern = score_tc_kernel<kFP8, kGather, kBeta, kH>;
@@ -771,19 +833,20 @@ cudaError_t launch_t(const CUtensorMap &tmA, const CUtensorMap &tmB, const Score
         grid = c.U;
     if (grid <= 0)
         return cudaSuccess;
-    return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(Roles<kGather>::kThreads),
-                      static_cast<size_t>(smem_bytes), s, tmA, tmB, p, c);
+    return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(Roles<kGather, kH>::kThreads),
+                      static_cast<size_t>(smem_bytes), s, tmA, tmB, tmS, p, c);
 }
 
 template <bool kFP8, bool kGather, bool kBeta>
-cudaError_t dispatch_h(const CUtensorMap &tmA, const CUtensorMap &tmB, const ScoreParams &p,
+cudaError_t dispatch_h(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmS,
+                       const ScoreParams &p,
                        const TcConfig &c, int smem_bytes, cudaStream_t s)
 {
     switch (p.H) {
-    case 16: return launch_t<kFP8, kGather, kBeta, 16>(tmA, tmB, p, c, smem_bytes, s);
-    case 32: return launch_t<kFP8, kGather, kBeta, 32>(tmA, tmB, p, c, smem_bytes, s);
-    case 64: return launch_t<kFP8, kGather, kBeta, 64>(tmA, tmB, p, c, smem_bytes, s);
-    case 128: return launch_t<kFP8, kGather, kBeta, 128>(tmA, tmB, p, c, smem_bytes, s);
+    case 16: return launch_t<kFP8, kGather, kBeta, 16>(tmA, tmB, tmS, p, c, smem_bytes, s);
+    case 32: return launch_t<kFP8, kGather, kBeta, 32>(tmA, tmB, tmS, p, c, smem_bytes, s);
+    case 64: return launch_t<kFP8, kGather, kBeta, 64>(tmA, tmB, tmS, p, c, smem_bytes, s);
+    case 128: return launch_t<kFP8, kGather, kBeta, 128>(tmA, tmB, tmS, p, c, smem_bytes, s);
     default: return cudaErrorInvalidValue;
     }
 }
@@ -857,7 +920,7 @@ cudaError_t launch_score_tc(const ScoreParams &p, cudaStream_t s)
     const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const CUtensorMapSwizzle swz = fp8 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
 
-    CUtensorMap tmA, tmB;
+    CUtensorMap tmA, tmB, tmS;
     // latent [B][L][r] as a 3D map {r, L, B}; box {64, 128, 1}
     {
         cuuint64_t dims[3] = {static_cast<cuuint64_t>(p.r), static_cast<cuuint64_t>(p.L_lat),
@@ -883,19 +946,31 @@ cudaError_t launch_score_tc(const ScoreParams &p, cudaStream_t s)
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
+    // token scales [B][L] fp32 as a 2D map {L, B}; box {128, 1} (one tile's scales)
+    memset(&tmS, 0, sizeof tmS);
+    if (c.sc_stage) {
+        cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.L_lat), static_cast<cuuint64_t>(p.B)};
+        cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.L_lat) * 4};
+        cuuint32_t box[2] = {kTileM, 1};
+        cuuint32_t estr[2] = {1, 1};
+        if (enc(&tmS, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(p.lat_scale), dims, strides,
+                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
     const bool beta = p.beta != nullptr;
     if (fp8) {
         if (gather)
-            return beta ? dispatch_h<true, true, true>(tmA, tmB, p, c, smem_bytes, s)
-                        : dispatch_h<true, true, false>(tmA, tmB, p, c, smem_bytes, s);
-        return beta ? dispatch_h<true, false, true>(tmA, tmB, p, c, smem_bytes, s)
-                    : dispatch_h<true, false, false>(tmA, tmB, p, c, smem_bytes, s);
+            return beta ? dispatch_h<true, true, true>(tmA, tmB, tmS, p, c, smem_bytes, s)
+                        : dispatch_h<true, true, false>(tmA, tmB, tmS, p, c, smem_bytes, s);
+        return beta ? dispatch_h<true, false, true>(tmA, tmB, tmS, p, c, smem_bytes, s)
+                    : dispatch_h<true, false, false>(tmA, tmB, tmS, p, c, smem_bytes, s);
     }
     if (gather)
-        return beta ? dispatch_h<false, true, true>(tmA, tmB, p, c, smem_bytes, s)
-                    : dispatch_h<false, true, false>(tmA, tmB, p, c, smem_bytes, s);
-    return beta ? dispatch_h<false, false, true>(tmA, tmB, p, c, smem_bytes, s)
-                : dispatch_h<false, false, false>(tmA, tmB, p, c, smem_bytes, s);
+        return beta ? dispatch_h<false, true, true>(tmA, tmB, tmS, p, c, smem_bytes, s)
+                    : dispatch_h<false, true, false>(tmA, tmB, tmS, p, c, smem_bytes, s);
+    return beta ? dispatch_h<false, false, true>(tmA, tmB, tmS, p, c, smem_bytes, s)
+                : dispatch_h<false, false, false>(tmA, tmB, tmS, p, c, smem_bytes, s);
 }
 
 } // namespace li

@@ -221,6 +221,50 @@ def test_topk_two_pass_equals_one_pass(li, orc):
         np.testing.assert_array_equal(np.sort(v1.cpu().numpy(), axis=1), np.sort(v2.cpu().numpy(), axis=1))
 
 
+@pytest.mark.parametrize("L", [8193, 16384, 20000, 24577, 32768])
+def test_topk_rows_8k_to_32k_ragged_ties_and_valid_lengths(li, orc, L):
+    """Rows of 8K-32K scores: lengths off the 8K multiples, valid lengths
+    around 8K borders, and ties at the threshold across those borders (taken
+    by lowest position) are all bit-exact."""
+    g = torch.Generator().manual_seed(L)
+    s = torch.randn(8, L, generator=g) * 3 + 5
+    s[1] = torch.randint(0, 3, (L,), generator=g).float()               # heavy ties everywhere
+    s[2] = 7.0                                                          # one value
+    s[3, 8000:8400] = 50.0                                              # ties across the rank-0/1 border
+    s[4, ::2] = -0.0
+    s[5] = torch.rand(L, generator=g) * 1e-3 + 1.0                      # one narrow binade
+    vl = torch.tensor([L, L, 5000, 8192, 8191, L - 1, 3, 0], dtype=torch.int32)
+    for k in (1, 100, 2048, 8200):
+        for v in (None, vl):
+            gi, gv = _topk_gpu(li, s, k, v)
+            oi, ov = orc.topk(s.double().numpy(), k, valid_len=None if v is None else v.numpy())
+            exact_sets_equal(gi, oi)
+            np.testing.assert_array_equal(np.sort(gv, axis=1), np.sort(ov.astype(np.float32), axis=1))
+
+
+def test_topk_long_rows_with_valid_lengths_and_workspace(li, orc):
+    """Causal rows (a valid prefix per row) longer than 32,768 with a
+    workspace given: lengths at and around 32K segment borders, empty and
+    one-element prefixes, and ties across segment borders."""
+    g = torch.Generator().manual_seed(23)
+    L = 131072
+    s = torch.randn(8, L, generator=g) * 4 + 10
+    s[2] = torch.randint(0, 6, (L,), generator=g).float()
+    s[5, 30000:70000] = 99.0
+    vl = torch.tensor([L, 0, 1, 100, 32768, 32769, 70000, L - 1], dtype=torch.int32)
+    sd, vd = s.to(DEV), vl.to(DEV)
+    for k in (1, 2048, 8192):
+        ws = torch.empty(li.li_topk_workspace_size(8, L, k), dtype=torch.uint8, device=DEV)
+        i1 = torch.empty(8, k, dtype=torch.int32, device=DEV)
+        v1 = torch.empty(8, k, dtype=torch.float32, device=DEV)
+        assert li.li_topk(sd, k, i1, v1, vd, ws) == 0
+        _sync_ok(li)
+        oi, ov = orc.topk(s.double().numpy(), k, valid_len=vl.numpy())
+        gi, gv = i1.cpu().numpy(), v1.cpu().numpy()
+        exact_sets_equal(gi, oi)
+        np.testing.assert_array_equal(np.sort(gv, axis=1), np.sort(ov.astype(np.float32), axis=1))
+
+
 def test_topk_threshold_bin_overflows_shared_memory(li, orc):
     """Scores sharing their top 12 key bits (one exponent, same 3 mantissa bits) force the
     re-read path; a narrower cluster forces the second-digit re-read too."""
