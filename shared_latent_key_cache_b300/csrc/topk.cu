@@ -588,53 +588,46 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p)
 // are needed).
 
 constexpr int kRegPer = 32;
-constexpr int kRegRow = kRegPer * kThreads;
+constexpr int kRegRow = kRegPer * kThreads;     // longest row: 32 keys x 1024 threads
 constexpr int kRBins = 2048;
 
 constexpr int kRCap = 4096;       // candidate list (keys in the threshold bin)
 constexpr int kRankMax = 256;     // lists up to this long are ranked by counting
 
+template <int NT>
 struct RegSmem {
+    static constexpr int kNW = NT / 32;
     uint32_t hist[kRBins];
     uint32_t ckey[kRCap];
     int32_t cpos[kRCap];
-    uint32_t wa[kWarps];
-    uint32_t wb[kWarps];
+    uint32_t wa[kNW];
+    uint32_t wb[kNW];
     uint32_t kmin, kmax;
     int sel_bin;
     uint32_t sel_gt;
     int slot;
     uint32_t out_cnt, cand_cnt;
+    uint32_t scan_tot;        // block total of the last reg_excl_scan
 };
 
-// Warp-aggregated reservation of `n` consecutive slots per lane on a shared
-// counter; returns this lane's first slot.
-__device__ __forceinline__ uint32_t warp_reserve(uint32_t *counter, uint32_t n)
+// Largest bin b with  sum_{d >= b} hist[d] >= need; sets b and the count
+// strictly above it.  Thread t owns bins [B t, B t + B), B = 2048 / NT; the
+// suffix sums run as shuffles within warps and one shuffle scan of the warp
+// totals in warp 0.  All threads must call.
+template <int NT>
+__device__ void reg_select_bin(RegSmem<NT> &sm, uint32_t need, int &bin, uint32_t &gt)
 {
-    const int lane = threadIdx.x & 31;
-    uint32_t x = n;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const uint32_t y = __shfl_up_sync(0xffffffffu, x, off);
-        if (lane >= off)
-            x += y;
-    }
-    const uint32_t tot = __shfl_sync(0xffffffffu, x, 31);
-    uint32_t base = 0;
-    if (lane == 31 && tot > 0)
-        base = atomicAdd(counter, tot);
-    base = __shfl_sync(0xffffffffu, base, 31);
-    return base + x - n;
-}
-
-// Largest bin b (2 per thread) with  sum_{d >= b} hist[d] >= need; sets b and
-// the count strictly above it.  All threads must call.
-__device__ void reg_select_bin(RegSmem &sm, uint32_t need, int &bin, uint32_t &gt)
-{
+    constexpr int kB = kRBins / NT;
+    constexpr int kNW = NT / 32;
     const int t = threadIdx.x, lane = t & 31, w = t >> 5;
-    const uint32_t h0 = sm.hist[2 * t], h1 = sm.hist[2 * t + 1];
-    const uint32_t local = h0 + h1;
-    uint32_t x = local;
+    uint32_t h[kB];
+    uint32_t local = 0;
+#pragma unroll
+    for (int j = 0; j < kB; ++j) {
+        h[j] = sm.hist[kB * t + j];
+        local += h[j];
+    }
+    uint32_t x = local;                       // inclusive suffix within the warp
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
         const uint32_t y = __shfl_down_sync(0xffffffffu, x, off);
@@ -644,17 +637,28 @@ __device__ void reg_select_bin(RegSmem &sm, uint32_t need, int &bin, uint32_t &g
     if (lane == 0)
         sm.wa[w] = x;
     __syncthreads();
-    uint32_t s = x - local;
-    for (int w2 = w + 1; w2 < kWarps; ++w2)
-        s += sm.wa[w2];
-    if (s < need && s + h1 >= need) {
-        sm.sel_bin = 2 * t + 1;
-        sm.sel_gt = s;
+    if (w == 0) {
+        // exclusive suffix of the warp totals: keys in later warps' bins
+        const uint32_t tot = lane < kNW ? sm.wa[lane] : 0u;
+        uint32_t y = tot;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const uint32_t z = __shfl_down_sync(0xffffffffu, y, off);
+            if (lane + off < 32)
+                y += z;
+        }
+        if (lane < kNW)
+            sm.wb[lane] = y - tot;
     }
-    s += h1;
-    if (s < need && s + h0 >= need) {
-        sm.sel_bin = 2 * t;
-        sm.sel_gt = s;
+    __syncthreads();
+    uint32_t s = sm.wb[w] + (x - local);
+#pragma unroll
+    for (int j = kB - 1; j >= 0; --j) {
+        if (s < need && s + h[j] >= need) {
+            sm.sel_bin = kB * t + j;
+            sm.sel_gt = s;
+        }
+        s += h[j];
     }
     __syncthreads();
     bin = sm.sel_bin;
@@ -662,9 +666,12 @@ __device__ void reg_select_bin(RegSmem &sm, uint32_t need, int &bin, uint32_t &g
     __syncthreads();
 }
 
-// Exclusive prefix sum of v over the block (thread order); *total = block sum.
-__device__ __forceinline__ uint32_t reg_excl_scan(RegSmem &sm, uint32_t v, uint32_t *total)
+// Exclusive prefix sum of v over the block (thread order); *total = block
+// sum.  Shuffles within warps, one shuffle scan of the warp totals in warp 0.
+template <int NT>
+__device__ __forceinline__ uint32_t reg_excl_scan(RegSmem<NT> &sm, uint32_t v, uint32_t *total)
 {
+    constexpr int kNW = NT / 32;
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     uint32_t x = v;
 #pragma unroll
@@ -676,20 +683,32 @@ __device__ __forceinline__ uint32_t reg_excl_scan(RegSmem &sm, uint32_t v, uint3
     if (lane == 31)
         sm.wb[w] = x;
     __syncthreads();
-    uint32_t base = 0, tot = 0;
-    for (int w2 = 0; w2 < kWarps; ++w2) {
-        const uint32_t c = sm.wb[w2];
-        base += w2 < w ? c : 0u;
-        tot += c;
+    if (w == 0) {
+        const uint32_t tot = lane < kNW ? sm.wb[lane] : 0u;
+        uint32_t y = tot;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const uint32_t z = __shfl_up_sync(0xffffffffu, y, off);
+            if (lane >= off)
+                y += z;
+        }
+        if (lane < kNW)
+            sm.wa[lane] = y - tot;            // exclusive base of warp `lane`
+        if (lane == 31)
+            sm.scan_tot = y;                  // block total
     }
-    *total = tot;
+    __syncthreads();
+    const uint32_t base = sm.wa[w];
+    *total = sm.scan_tot;
     __syncthreads();
     return base + x - v;
 }
 
-__global__ void __launch_bounds__(kThreads, 1) topk_reg_kernel(const TopkParams p)
+template <int NT>
+__global__ void __launch_bounds__(NT, 1) topk_reg_kernel(const TopkParams p)
 {
-    __shared__ RegSmem sm;
+    constexpr int kNW = NT / 32;
+    __shared__ RegSmem<NT> sm;
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     griddep_wait();
     griddep_launch_dependents();
@@ -721,13 +740,13 @@ __global__ void __launch_bounds__(kThreads, 1) topk_reg_kernel(const TopkParams 
         // output index of row position pos (map and pos_off are never both used)
         auto gpos = [&](int pos) -> int { return map ? map[pos] : pos + pos_off; };
 
-        for (int j = nsel + tid; j < p.k; j += kThreads) {      // padding
+        for (int j = nsel + tid; j < p.k; j += NT) {      // padding
             oidx[j] = p.pad_idx;
             if (oval)
                 oval[j] = -__int_as_float(0x7f800000);
         }
         if (nsel == V) {
-            for (int j = tid; j < V; j += kThreads) {
+            for (int j = tid; j < V; j += NT) {
                 oidx[j] = gpos(j);
                 if (oval)
                     oval[j] = src[j];
@@ -736,7 +755,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_reg_kernel(const TopkParams 
             continue;
         }
 
-        // ---- load: element e of this thread is at position 4 (tid + 1024 (e / 4)) + e % 4
+        // ---- load: element e of this thread is at position 4 (tid + NT (e / 4)) + e % 4
         uint32_t key[kRegPer];
         const bool al16 = (reinterpret_cast<uintptr_t>(src) & 15u) == 0;
         if (al16 && (Lr & 3) == 0) {
@@ -747,7 +766,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_reg_kernel(const TopkParams 
             float4 v[kRegPer / 4];
 #pragma unroll
             for (int i = 0; i < kRegPer / 4; ++i) {
-                const int q = tid + kThreads * i;
+                const int q = tid + NT * i;
                 v[i] = 4 * q < Lr ? __ldg(r4 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
 #pragma unroll
@@ -760,14 +779,14 @@ __global__ void __launch_bounds__(kThreads, 1) topk_reg_kernel(const TopkParams 
         } else {
 #pragma unroll
             for (int i = 0; i < kRegPer / 4; ++i) {
-                const int pos = 4 * (tid + kThreads * i);
+                const int pos = 4 * (tid + NT * i);
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
                     key[4 * i + j] = pos + j < V ? float_key(__ldg(src + pos + j)) : 0u;
             }
         }
-        const bool full = V == kRegRow;
-        auto valid = [&](int e) { return full || 4 * (tid + kThreads * (e >> 2)) + (e & 3) < V; };
+        const bool full = V == kRegPer * NT;
+        auto valid = [&](int e) { return full || 4 * (tid + NT * (e >> 2)) + (e & 3) < V; };
 
         // ---- key range of the row
         uint32_t lo = 0xFFFFFFFFu, hi = 0u;
@@ -784,17 +803,16 @@ __global__ void __launch_bounds__(kThreads, 1) topk_reg_kernel(const TopkParams 
             sm.wb[w] = hi;
         }
         __syncthreads();
-        if (tid == 0) {
-            uint32_t a = 0xFFFFFFFFu, b = 0u;
-            for (int w2 = 0; w2 < kWarps; ++w2) {
-                a = min(a, sm.wa[w2]);
-                b = max(b, sm.wb[w2]);
+        if (w == 0) {
+            const uint32_t a = __reduce_min_sync(0xffffffffu, lane < kNW ? sm.wa[lane] : 0xFFFFFFFFu);
+            const uint32_t b = __reduce_max_sync(0xffffffffu, lane < kNW ? sm.wb[lane] : 0u);
+            if (lane == 0) {
+                sm.kmin = a;
+                sm.kmax = b;
+                sm.slot = 0;
+                sm.out_cnt = 0;
+                sm.cand_cnt = 0;
             }
-            sm.kmin = a;
-            sm.kmax = b;
-            sm.slot = 0;
-            sm.out_cnt = 0;
-            sm.cand_cnt = 0;
         }
         __syncthreads();
         const uint32_t kmin = sm.kmin;
@@ -809,7 +827,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_reg_kernel(const TopkParams 
         uint32_t cnt_eq = 0;     // keys equal to it
         {
             // level 1: bits [shift1, nbits)
-            for (int i = tid; i < kRBins; i += kThreads)
+            for (int i = tid; i < kRBins; i += NT)
                 sm.hist[i] = 0u;
             __syncthreads();
 #pragma unroll
@@ -843,14 +861,18 @@ __global__ void __launch_bounds__(kThreads, 1) topk_reg_kernel(const TopkParams 
                 }
             }
             n_cand -= n_sure;
-            uint32_t so = warp_reserve(&sm.out_cnt, n_sure);
-            uint32_t co = warp_reserve(&sm.cand_cnt, n_cand);
+            // output slots by one block scan of (keys above, keys in the bin),
+            // packed 16 + 16 bits (each count is at most 32,768)
+            uint32_t both_tot = 0;
+            const uint32_t both = reg_excl_scan(sm, (n_sure << 16) | n_cand, &both_tot);
+            uint32_t so = both >> 16;
+            uint32_t co = both & 0xFFFFu;
             if (map == nullptr && oval == nullptr) {
 #pragma unroll
                 for (int e = 0; e < kRegPer; ++e) {
                     const uint32_t o = key[e] - kmin;
                     if (valid(e) && o >= lo_off) {
-                        const int pos = 4 * (tid + kThreads * (e >> 2)) + (e & 3);
+                        const int pos = 4 * (tid + NT * (e >> 2)) + (e & 3);
                         if (o > hi_off) {
                             oidx[so] = pos + pos_off;
                             ++so;
@@ -866,7 +888,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_reg_kernel(const TopkParams 
                 for (int e = 0; e < kRegPer; ++e) {
                     const uint32_t o = key[e] - kmin;
                     if (valid(e) && o >= lo_off) {
-                        const int pos = 4 * (tid + kThreads * (e >> 2)) + (e & 3);
+                        const int pos = 4 * (tid + NT * (e >> 2)) + (e & 3);
                         if (o > hi_off) {
                             oidx[so] = gpos(pos);
                             if (oval)
@@ -887,27 +909,31 @@ __global__ void __launch_bounds__(kThreads, 1) topk_reg_kernel(const TopkParams 
                 // order is the number of candidates ahead of it, counted by four
                 // threads over a quarter of the list each; the `need` lowest
                 // ranks are taken, rank r into output slot gt1 + r.
-                const int c = tid >> 2, part = tid & 3;
+                const int part = tid & 3;
                 const int per = (n + 3) >> 2;
-                uint32_t ahead = 0, ck = 0;
-                int cp = 0;
-                if (c < n) {
-                    ck = sm.ckey[c];
-                    cp = sm.cpos[c];
-                    const int j1 = min(n, (part + 1) * per);
-                    for (int j = part * per; j < j1; ++j) {
-                        const uint32_t kj = sm.ckey[j];
-                        const int pj = sm.cpos[j];
-                        ahead += (kj > ck || (kj == ck && pj < cp)) ? 1u : 0u;
+                // NT / 4 candidates per round (one round at 1024 threads)
+                for (int c0r = 0; c0r < n; c0r += NT / 4) {
+                    const int c = c0r + (tid >> 2);
+                    uint32_t ahead = 0, ck = 0;
+                    int cp = 0;
+                    if (c < n) {
+                        ck = sm.ckey[c];
+                        cp = sm.cpos[c];
+                        const int j1 = min(n, (part + 1) * per);
+                        for (int j = part * per; j < j1; ++j) {
+                            const uint32_t kj = sm.ckey[j];
+                            const int pj = sm.cpos[j];
+                            ahead += (kj > ck || (kj == ck && pj < cp)) ? 1u : 0u;
+                        }
                     }
-                }
-                ahead += __shfl_xor_sync(0xffffffffu, ahead, 1);
-                ahead += __shfl_xor_sync(0xffffffffu, ahead, 2);
-                if (c < n && part == 0 && ahead < need) {
-                    const uint32_t sl = gt1 + ahead;
-                    oidx[sl] = cp;
-                    if (oval)
-                        oval[sl] = key_float(ck);
+                    ahead += __shfl_xor_sync(0xffffffffu, ahead, 1);
+                    ahead += __shfl_xor_sync(0xffffffffu, ahead, 2);
+                    if (c < n && part == 0 && ahead < need) {
+                        const uint32_t sl = gt1 + ahead;
+                        oidx[sl] = cp;
+                        if (oval)
+                            oval[sl] = key_float(ck);
+                    }
                 }
                 __syncthreads();
                 continue;
@@ -918,10 +944,10 @@ __global__ void __launch_bounds__(kThreads, 1) topk_reg_kernel(const TopkParams 
                 if (hs == 0)
                     break;
                 const uint32_t msk = (1u << (hs - ls)) - 1u;
-                for (int i = tid; i < kRBins; i += kThreads)
+                for (int i = tid; i < kRBins; i += NT)
                     sm.hist[i] = 0u;
                 __syncthreads();
-                for (int i = tid; i < n; i += kThreads) {
+                for (int i = tid; i < n; i += NT) {
                     const uint32_t o = sm.ckey[i] - kmin;
                     if ((o >> hs) == (T >> hs))
                         atomicAdd(&sm.hist[(o >> ls) & msk], 1u);
@@ -939,7 +965,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_reg_kernel(const TopkParams 
             if (tid == 0)
                 sm.slot = 0;
             __syncthreads();
-            for (int i = tid; i < n; i += kThreads) {
+            for (int i = tid; i < n; i += NT) {
                 if (sm.ckey[i] > K) {
                     const uint32_t sl = gt1 + static_cast<uint32_t>(atomicAdd(&sm.slot, 1));
                     oidx[sl] = sm.cpos[i];
@@ -957,10 +983,10 @@ __global__ void __launch_bounds__(kThreads, 1) topk_reg_kernel(const TopkParams 
                     const int hs = lv == 0 ? 21 : (lv == 1 ? 10 : 0);
                     const int ws = lv == 2 ? 10 : 11;
                     const uint32_t pm = lv == 0 ? 0u : (0xFFFFFFFFu << (hs + ws));
-                    for (int i = tid; i < kRBins; i += kThreads)
+                    for (int i = tid; i < kRBins; i += NT)
                         sm.hist[i] = 0u;
                     __syncthreads();
-                    for (int i = tid; i < n; i += kThreads) {
+                    for (int i = tid; i < n; i += NT) {
                         const uint32_t up = static_cast<uint32_t>(sm.cpos[i]);
                         if (sm.ckey[i] == K && (up & pm) == (P & pm))
                             atomicAdd(&sm.hist[kRBins - 1 - ((up >> hs) & ((1u << ws) - 1u))], 1u);
@@ -978,7 +1004,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_reg_kernel(const TopkParams 
             if (tid == 0)
                 sm.slot = 0;
             __syncthreads();
-            for (int i = tid; i < n; i += kThreads) {
+            for (int i = tid; i < n; i += NT) {
                 const int pos = sm.cpos[i];
                 if (sm.ckey[i] == K && static_cast<uint32_t>(pos) <= pmax) {
                     const uint32_t sl = eq_base + static_cast<uint32_t>(atomicAdd(&sm.slot, 1));
@@ -993,7 +1019,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_reg_kernel(const TopkParams 
         if (shift1 > 0) {
             // level 2: bits [shift2, shift1) of keys in the level-1 bin
             const uint32_t m2 = (1u << (shift1 - shift2)) - 1u;
-            for (int i = tid; i < kRBins; i += kThreads)
+            for (int i = tid; i < kRBins; i += NT)
                 sm.hist[i] = 0u;
             __syncthreads();
 #pragma unroll
@@ -1013,7 +1039,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_reg_kernel(const TopkParams 
         if (shift2 > 0) {
             // level 3: bits [0, shift2) of keys matching the first two digits
             const uint32_t m3 = (1u << shift2) - 1u;
-            for (int i = tid; i < kRBins; i += kThreads)
+            for (int i = tid; i < kRBins; i += NT)
                 sm.hist[i] = 0u;
             __syncthreads();
 #pragma unroll
@@ -1042,7 +1068,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_reg_kernel(const TopkParams 
 #pragma unroll
         for (int e = 0; e < kRegPer; ++e) {
             if (valid(e) && key[e] > K) {
-                const int pos = 4 * (tid + kThreads * (e >> 2)) + (e & 3);
+                const int pos = 4 * (tid + NT * (e >> 2)) + (e & 3);
                 oidx[slot] = gpos(pos);
                 if (oval)
                     oval[slot] = key_float(key[e]);
@@ -1054,7 +1080,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_reg_kernel(const TopkParams 
 #pragma unroll
             for (int e = 0; e < kRegPer; ++e) {
                 if (valid(e) && key[e] == K) {
-                    const int pos = 4 * (tid + kThreads * (e >> 2)) + (e & 3);
+                    const int pos = 4 * (tid + NT * (e >> 2)) + (e & 3);
                     const int s2 = static_cast<int>(sure) + atomicAdd(&sm.slot, 1);
                     oidx[s2] = gpos(pos);
                     if (oval)
@@ -1071,13 +1097,13 @@ __global__ void __launch_bounds__(kThreads, 1) topk_reg_kernel(const TopkParams 
                 const int hs = lv == 0 ? 21 : (lv == 1 ? 10 : 0);
                 const int ws = lv == 2 ? 10 : 11;
                 const uint32_t pm = lv == 0 ? 0u : (0xFFFFFFFFu << (hs + ws));
-                for (int i = tid; i < kRBins; i += kThreads)
+                for (int i = tid; i < kRBins; i += NT)
                     sm.hist[i] = 0u;
                 __syncthreads();
 #pragma unroll
                 for (int e = 0; e < kRegPer; ++e) {
                     if (valid(e) && key[e] == K) {
-                        const uint32_t up = static_cast<uint32_t>(map[4 * (tid + kThreads * (e >> 2)) + (e & 3)]);
+                        const uint32_t up = static_cast<uint32_t>(map[4 * (tid + NT * (e >> 2)) + (e & 3)]);
                         if ((up & pm) == (P & pm))
                             atomicAdd(&sm.hist[kRBins - 1 - ((up >> hs) & ((1u << ws) - 1u))], 1u);
                     }
@@ -1095,7 +1121,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_reg_kernel(const TopkParams 
 #pragma unroll
             for (int e = 0; e < kRegPer; ++e) {
                 if (valid(e) && key[e] == K) {
-                    const int up = map[4 * (tid + kThreads * (e >> 2)) + (e & 3)];
+                    const int up = map[4 * (tid + NT * (e >> 2)) + (e & 3)];
                     if (static_cast<uint32_t>(up) <= P) {
                         const int s2 = static_cast<int>(sure) + atomicAdd(&sm.slot, 1);
                         oidx[s2] = up;
@@ -1119,7 +1145,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_reg_kernel(const TopkParams 
                     const int e = 4 * i + j;
                     if (valid(e) && key[e] == K) {
                         if (r < need) {
-                            const int pos = 4 * (tid + kThreads * i) + j;
+                            const int pos = 4 * (tid + NT * i) + j;
                             oidx[sure + r] = gpos(pos);
                             if (oval)
                                 oval[sure + r] = key_float(K);
@@ -1157,8 +1183,19 @@ cudaError_t launch_topk(const TopkParams &p, cudaStream_t s)
     }
     const int64_t grid = p.rows < 0x7FFFFFFF ? p.rows : 0x7FFFFFFF;
     static_assert(kRegRow == kTopkRegRow, "register-resident row length");
-    if (p.segs > 1 || p.L_row <= kRegRow)
-        return launch_pdl(topk_reg_kernel, dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, s, p);
+    if (p.segs > 1 || p.L_row <= kRegRow) {
+        // as many threads as the row needs at 32 keys each (at least 128).
+        // Rows indexing a candidate list keep 1024 threads: every selected
+        // key's output is a dependent load from the list, fewer per thread.
+        const int Lr = p.map != nullptr ? kRegRow : (p.segs > 1 ? p.seg_len : p.L_row);
+        if (Lr <= 32 * 128)
+            return launch_pdl(topk_reg_kernel<128>, dim3(static_cast<unsigned>(grid)), dim3(128), 0, s, p);
+        if (Lr <= 32 * 256)
+            return launch_pdl(topk_reg_kernel<256>, dim3(static_cast<unsigned>(grid)), dim3(256), 0, s, p);
+        if (Lr <= 32 * 512)
+            return launch_pdl(topk_reg_kernel<512>, dim3(static_cast<unsigned>(grid)), dim3(512), 0, s, p);
+        return launch_pdl(topk_reg_kernel<1024>, dim3(static_cast<unsigned>(grid)), dim3(1024), 0, s, p);
+    }
     return launch_pdl(topk_kernel, dim3(static_cast<unsigned>(grid)), dim3(kThreads), static_cast<size_t>(smem), s, p);
 }
 
