@@ -702,19 +702,18 @@ def side_timings(a, w, x, step, li, stream, flush, dev):
                                   hidx, wsb, None, stream)
             assert st == 0
         hs_us = timeit(hs)
-        # per launch: absorb first, then the five launches of the selection between events
+        # per launch: absorb first, then the four launches of the selection between events
         stages = []
         for i in range(reps):
             flush()
-            ev = [torch.cuda.Event(enable_timing=True) for _ in range(7)]
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
             ev[0].record(stream)
             assert li.li_absorb_queries(x["q"], x["D"], q_abs, q_scale, stream) == 0
             assert li.li_hs_select_profiled(x["latent"], x["lat_scale"], q_abs, q_scale, x["w"], m, k,
                                             cand, hidx, wsb, ev[1:], None, stream) == 0
             stages.append(ev)
         torch.cuda.synchronize(dev)
-        names = ["absorb", "anchor_scan", "anchor_top_m", "anchor_top_k", "follower_rescore",
-                 "follower_top_k"]
+        names = ["absorb", "anchor_scan", "anchor_top_m", "follower_rescore", "top_k_all_layers"]
         per = {nm: statistics.median(e[j].elapsed_time(e[j + 1]) * 1e3 for e in stages)
                for j, nm in enumerate(names)}
         out["hs"] = {"m": m, "latency_us": hs_us, "stages_us": per,

@@ -137,6 +137,9 @@ size_t li_topk_workspace_size(int64_t rows, int L, int k);
  *          top-k of each 32,768-score segment, then of the segments'
  *          candidates, ties by position) with more parallelism.  The result
  *          is the same with or without it; NULL / too small = one pass.
+ *          Few rows (ceil(L / 8,192) * rows at most the SM count, L <=
+ *          131,072) are instead each spread over a thread-block cluster,
+ *          with or without ws.
  * Limits: 1 <= k <= 2^30, L < 2^31.
  */
 int li_topk(const float *scores, int64_t rows, int L, const int32_t *valid_len, int k,
@@ -174,13 +177,14 @@ int li_hs_select(const void *latent, int lat_t, const float *lat_scale,
 /*
  * li_hs_select with per-launch timing (a diagnostic entry point; the pages
  * have no counterpart).  Same arguments, work and results as li_hs_select,
- * plus `events`: six caller-created cudaEvent_t handles.  events[i] is
- * recorded on `stream` before launch i of the selection and events[5] after
- * the last one: 0 anchor scan, 1 anchor top-m (candidates), 2 anchor top-k,
- * 3 follower rescoring of the candidates, 4 follower top-k (with G = 1 the
- * last three intervals are empty).  Recording an event between two launches
- * ends their programmatic launch overlap, so the intervals add up to a little
- * more than an unprofiled call.  LI_ERR_INVALID_ARG when events is NULL.
+ * plus `events`: five caller-created cudaEvent_t handles.  events[i] is
+ * recorded on `stream` before launch i of the selection and events[4] after
+ * the last one: 0 anchor scan, 1 anchor top-m (candidates and their anchor
+ * scores), 2 follower rescoring of the candidates (empty interval when
+ * G = 1), 3 the top-k of every layer inside the candidates (one launch).
+ * Recording an event between two launches ends their programmatic launch
+ * overlap, so the intervals add up to a little more than an unprofiled call.
+ * LI_ERR_INVALID_ARG when events is NULL.
  */
 int li_hs_select_profiled(const void *latent, int lat_t, const float *lat_scale,
                           const void *q_abs, int abs_t, const float *q_abs_scale,

@@ -177,7 +177,7 @@ def li_hs_select(latent, lat_scale, q_abs, q_abs_scale, w, m: int, k: int, cand,
 
 def li_hs_select_profiled(latent, lat_scale, q_abs, q_abs_scale, w, m: int, k: int, cand, idx, ws,
                           events, beta=None, stream=None) -> int:
-    """li_hs_select with six torch.cuda.Event objects recorded around its five launches.
+    """li_hs_select with five torch.cuda.Event objects recorded around its four launches.
     torch creates an event's CUDA handle on its first record, so each event is
     recorded once here (on the same stream) before the library records it again."""
     B, L, r = latent.shape
@@ -185,7 +185,7 @@ def li_hs_select_profiled(latent, lat_scale, q_abs, q_abs_scale, w, m: int, k: i
     st = stream if stream is not None else torch.cuda.current_stream()
     for e in events:
         e.record(st)
-    arr = (ctypes.c_void_p * 6)(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    arr = (ctypes.c_void_p * 5)(*[ctypes.c_void_p(e.cuda_event) for e in events])
     return _lib.li_hs_select_profiled(
         _ptr(latent), _dtype_code(latent), _ptr(lat_scale), _ptr(q_abs), _dtype_code(q_abs),
         _ptr(q_abs_scale), _ptr(w), _ptr(beta), B, G, H, r, L, m, k, _ptr(cand), _ptr(idx),

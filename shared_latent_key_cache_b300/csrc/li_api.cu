@@ -79,6 +79,7 @@ cudaError_t launch_topk_two_pass(const TopkParams &p, void *ws, cudaStream_t s)
     a.rows = p.rows * S;
     a.idx = ci;
     a.vals = cv;
+    a.vals_stride = 0;
     a.rows_per_group = 1;
     a.group_stride = 1;
     a.row_offset = 0;
@@ -310,7 +311,7 @@ int li_topk(const float *scores, int64_t rows, int L, const int32_t *valid_len, 
     if (!p.status)
         return LI_ERR_CUDA;
     const size_t two = topk_two_pass_bytes(rows, L, k);
-    if (ws && two > 0 && ws_bytes >= two && !valid_len)
+    if (ws && two > 0 && ws_bytes >= two && !valid_len && !topk_cluster_path(p))
         return cuda_status(launch_topk_two_pass(p, ws, static_cast<cudaStream_t>(stream)));
     return cuda_status(launch_topk(p, static_cast<cudaStream_t>(stream)));
 }
@@ -320,9 +321,8 @@ size_t li_hs_workspace_size(int B, int G, int L, int m, int k)
     if (B <= 0 || G <= 0 || L <= 0 || m <= 0 || k <= 0)
         return 0;
     const size_t anchor = align256(sizeof(float) * static_cast<size_t>(B) * L);
-    const size_t cvals = align256(sizeof(float) * static_cast<size_t>(B) * m);
-    const size_t fol = align256(sizeof(float) * static_cast<size_t>(B) * (G - 1) * m);
-    return anchor + cvals + fol + topk_two_pass_bytes(B, L, m);
+    const size_t cand_scores = align256(sizeof(float) * static_cast<size_t>(B) * G * m);
+    return anchor + cand_scores + topk_two_pass_bytes(B, L, m);
 }
 
 } // extern "C"
@@ -346,8 +346,10 @@ int hs_check_args(const void *latent, int lat_t, const float *lat_scale, const v
 
 namespace {
 
-// The five launches of hierarchical selection; when `ev` is given, ev[i] is
-// recorded on the stream before launch i and ev[5] after the last one.
+// The four launches of hierarchical selection (anchor scan, anchor top-m,
+// follower rescoring, every layer's top-k inside the candidates); when `ev`
+// is given, ev[i] is recorded on the stream before launch i and ev[4] after
+// the last one.
 int hs_select_impl(const void *latent, int lat_t, const float *lat_scale, const void *q_abs,
                    int abs_t, const float *q_abs_scale, const float *w, const float *beta, int B,
                    int G, int H, int r, int L, int m, int k, int32_t *cand, int32_t *idx, void *ws,
@@ -363,13 +365,14 @@ int hs_select_impl(const void *latent, int lat_t, const float *lat_scale, const 
     if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
         return LI_ERR_ALIGNMENT;
 
+    // workspace: anchor scores [B][L], then the candidates' scores of every
+    // layer [B][G][m] (row 0 the anchor's, from the top-m pass; rows 1..G-1
+    // the followers' rescoring), then the top-m pass's own scratch
     uint8_t *wsb = static_cast<uint8_t *>(ws);
     float *anchor = reinterpret_cast<float *>(wsb);
-    float *cvals = reinterpret_cast<float *>(wsb + align256(sizeof(float) * static_cast<size_t>(B) * L));
-    float *fol = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(cvals) +
-                                           align256(sizeof(float) * static_cast<size_t>(B) * m));
-    void *tws = reinterpret_cast<uint8_t *>(fol) +
-                align256(sizeof(float) * static_cast<size_t>(B) * (G - 1) * m);   // anchor top-m passes
+    float *cs = reinterpret_cast<float *>(wsb + align256(sizeof(float) * static_cast<size_t>(B) * L));
+    void *tws = reinterpret_cast<uint8_t *>(cs) +
+                align256(sizeof(float) * static_cast<size_t>(B) * G * m);
     const int nc = m < L ? m : L;
 
     ScoreParams a{};
@@ -396,11 +399,13 @@ int hs_select_impl(const void *latent, int lat_t, const float *lat_scale, const 
     a.n_gather = 0;
     ScoreParams f = a;
     f.gather_idx = cand;
-    f.scores = fol;
+    f.scores = cs;
     f.g0 = 1;
     f.Gs = G - 1;
     f.L_out = m;
     f.n_gather = nc;
+    f.Gout = G;          // rows 1..G-1 of each sequence's [G][m] block
+    f.gout0 = 1;
     if (!score_supported(a) || (G > 1 && !score_supported(f)))
         return LI_ERR_UNSUPPORTED;
 
@@ -419,7 +424,7 @@ int hs_select_impl(const void *latent, int lat_t, const float *lat_scale, const 
     st = run_score(a, s);
     if (st != LI_OK)
         return st;
-    // 2. anchor top-m -> candidate set (and its scores)
+    // 2. anchor top-m -> candidate set, its scores into row 0 of [B][G][m]
     mark(1);
     TopkParams t{};
     t.scores = anchor;
@@ -429,51 +434,44 @@ int hs_select_impl(const void *latent, int lat_t, const float *lat_scale, const 
     t.valid_len = nullptr;
     t.k = m;
     t.idx = cand;
-    t.vals = cvals;
+    t.vals = cs;
+    t.vals_stride = static_cast<int64_t>(G) * m;
     t.rows_per_group = 1;
     t.group_stride = 1;
     t.row_offset = 0;
     t.map = nullptr;
     t.map_stride = 0;
     t.status = status;
-    st = cuda_status(topk_two_pass_bytes(B, L, m) > 0 ? launch_topk_two_pass(t, tws, s)
-                                                      : launch_topk(t, s));
+    st = cuda_status(topk_two_pass_bytes(B, L, m) > 0 && !topk_cluster_path(t)
+                         ? launch_topk_two_pass(t, tws, s)
+                         : launch_topk(t, s));
     if (st != LI_OK)
         return st;
-    // 3. the anchor's own top-k, inside its candidates
+    // 3. followers rescore the candidate rows of the latent (rows 1..G-1)
     mark(2);
-    TopkParams ta = t;
-    ta.scores = cvals;
-    ta.in_stride = m;
-    ta.L_row = nc;
-    ta.k = k;
-    ta.idx = idx;
-    ta.vals = nullptr;
-    ta.group_stride = G;
-    ta.map = cand;
-    ta.map_stride = m;
-    st = cuda_status(launch_topk(ta, s));
-    if (st != LI_OK || G == 1) {
-        mark(3);
-        mark(4);
-        mark(5);
-        return st;
+    if (G > 1) {
+        st = run_score(f, s);
+        if (st != LI_OK)
+            return st;
     }
-    // 4. followers rescore the candidate rows of the latent
+    // 4. every layer's top-k inside the candidates, one launch over B x G rows
     mark(3);
-    st = run_score(f, s);
-    if (st != LI_OK)
-        return st;
-    // 5. followers' top-k inside the candidates
+    TopkParams tk = t;
+    tk.scores = cs;
+    tk.rows = static_cast<int64_t>(B) * G;
+    tk.in_stride = m;
+    tk.L_row = nc;
+    tk.k = k;
+    tk.idx = idx;
+    tk.vals = nullptr;
+    tk.vals_stride = 0;
+    tk.rows_per_group = G;
+    tk.group_stride = G;
+    tk.row_offset = 0;
+    tk.map = cand;
+    tk.map_stride = m;
+    st = cuda_status(launch_topk(tk, s));
     mark(4);
-    TopkParams tf = ta;
-    tf.scores = fol;
-    tf.rows = static_cast<int64_t>(B) * (G - 1);
-    tf.rows_per_group = G - 1;
-    tf.group_stride = G;
-    tf.row_offset = 1;
-    st = cuda_status(launch_topk(tf, s));
-    mark(5);
     return st;
 }
 
@@ -499,8 +497,8 @@ int li_hs_select_profiled(const void *latent, int lat_t, const float *lat_scale,
 {
     if (!events)
         return LI_ERR_INVALID_ARG;
-    cudaEvent_t ev[6];
-    for (int i = 0; i < 6; ++i)
+    cudaEvent_t ev[5];
+    for (int i = 0; i < 5; ++i)
         ev[i] = static_cast<cudaEvent_t>(events[i]);
     return hs_select_impl(latent, lat_t, lat_scale, q_abs, abs_t, q_abs_scale, w, beta, B, G, H, r,
                           L, m, k, cand, idx, ws, ws_bytes, stream, ev);

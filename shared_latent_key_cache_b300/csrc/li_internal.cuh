@@ -108,8 +108,13 @@ struct TopkParams {
     int segs = 1;
     int seg_len = 0;
     int pad_idx = -1;   // index written to output slots past min(k, V)
+    int64_t vals_stride = 0;   // floats between out rows of vals (0: k)
 };
 cudaError_t launch_topk(const TopkParams &p, cudaStream_t s);
+// True when launch_topk spreads each row over a thread-block cluster (few
+// rows longer than 8,192 scores, no candidate list, no segments): the
+// two-pass workspace path is then not needed.
+bool topk_cluster_path(const TopkParams &p);
 // Longest row (and segment) the register-resident top-k takes.
 constexpr int kTopkRegRow = 32768;
 

@@ -12,7 +12,10 @@
 //
 // Rows of at most 32,768 scores take the register-resident path below (one
 // read of the row, three histogram levels over the keys held in registers).
-// Longer rows: one 1024-thread CTA per row, no global scratch memory:
+// A few rows longer than 8,192 scores (all CTAs one per SM) are each spread
+// over a thread-block cluster that merges its histograms in distributed
+// shared memory (the cluster path, further below).
+// Other long rows: one 1024-thread CTA per row, no global scratch memory:
 //  1. Sampled thresholds (rows of >= 8192 valid scores selecting at most about
 //     a quarter of them): 4096 stratified samples are histogrammed (12 + 12
 //     key bits) to find two keys whose sample ranks sit five standard
@@ -340,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p)
         const int64_t orow = grp * p.group_stride + row % p.rows_per_group + p.row_offset;
         RowOut o;
         o.idx = p.idx + orow * p.k;
-        o.val = p.vals ? p.vals + orow * p.k : nullptr;
+        o.val = p.vals ? p.vals + orow * (p.vals_stride ? p.vals_stride : p.k) : nullptr;
         o.map = p.map ? p.map + grp * p.map_stride : nullptr;
         o.k = p.k;
         const int nsel = p.k < V ? p.k : V;
@@ -734,7 +737,7 @@ __global__ void __launch_bounds__(NT, 1) topk_reg_kernel(const TopkParams p)
         const int64_t grp = row / p.rows_per_group;
         const int64_t orow = grp * p.group_stride + row % p.rows_per_group + p.row_offset;
         int32_t *oidx = p.idx + orow * p.k;
-        float *oval = p.vals ? p.vals + orow * p.k : nullptr;
+        float *oval = p.vals ? p.vals + orow * (p.vals_stride ? p.vals_stride : p.k) : nullptr;
         const int32_t *map = p.map ? p.map + grp * p.map_stride : nullptr;
         const int nsel = p.k < V ? p.k : V;
         // output index of row position pos (map and pos_off are never both used)
@@ -1162,18 +1165,632 @@ __global__ void __launch_bounds__(NT, 1) topk_reg_kernel(const TopkParams p)
     }
 }
 
+// ------------------------------------------------------------------------
+// Cluster path for a few long rows (up to 16 x 32 x NT scores): one row is
+// spread over a thread-block cluster, each CTA holding 32 keys per thread
+// in registers, so that a handful of rows still occupies every SM.  The
+// row's key histogram is merged level by level (key bits [21, 32), then
+// [9, 21) inside the level-1 bin) in the first CTA's shared memory through
+// distributed shared memory; the first CTA finds the threshold digit and
+// writes it into every CTA.  Keys above the 23-bit threshold prefix are
+// written by the CTA that holds them.  The few keys sharing the prefix are
+// gathered in the first CTA and ranked there (key desc, position asc).  If
+// there are many of them (near-equal scores), bits [0, 9) take a third
+// merged level and the keys equal to the exact threshold are split between
+// CTAs by position: every position of CTA c precedes those of CTA c + 1.
+
+constexpr int kCB1 = 2048;       // level-1 bins: key bits [21, 32)
+constexpr int kCB2 = 4096;       // level-2 bins: key bits [9, 21)
+constexpr int kCB3 = 512;        // level-3 bins: key bits [0, 9)
+constexpr int kCList = 256;      // prefix-sharing keys ranked in the first CTA
+constexpr int kClusterMax = 16;
+
+template <int NT>
+struct ClusterSmem {
+    static constexpr int kNW = NT / 32;
+    uint32_t loc[kCB2];          // this CTA's histogram; first CTA: then the candidate list
+    uint32_t m1[kCB1];           // merged histograms (first CTA)
+    uint32_t m2[kCB2];
+    uint32_t m3[kCB3];
+    uint32_t tie[kClusterMax];   // keys equal to the threshold, per CTA (first CTA)
+    uint32_t slot;               // output slots handed out (first CTA)
+    uint32_t ncand;              // candidates listed (first CTA)
+    uint32_t res[3];             // threshold digit, count above its bin, count in it
+    uint32_t wa[kNW], wb[kNW];
+    uint32_t scan_tot;
+    uint32_t base_s, base_c;
+    int sel_bin;
+    uint32_t sel_gt;
+};
+
+__device__ __forceinline__ uint32_t cl_rank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cl_nrank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+
+// Every thread of every CTA of the cluster: prior memory accesses are
+// released to, and the peers' acquired from, the whole cluster.
+__device__ __forceinline__ void cl_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cl_arrive()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cl_wait()
+{
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Address of `local` (this CTA's shared memory) in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t cl_map(const void *local, uint32_t rank)
+{
+    uint32_t a;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(local)), "r"(rank));
+    return a;
+}
+
+__device__ __forceinline__ void cl_red_add(uint32_t addr, uint32_t v)
+{
+    asm volatile("red.relaxed.cluster.shared::cluster.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t cl_atom_add(uint32_t addr, uint32_t v)
+{
+    uint32_t old;
+    asm volatile("atom.relaxed.cluster.shared::cluster.add.u32 %0, [%1], %2;"
+                 : "=r"(old) : "r"(addr), "r"(v) : "memory");
+    return old;
+}
+
+__device__ __forceinline__ void cl_st(uint32_t addr, uint32_t v)
+{
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t cl_ld(uint32_t addr)
+{
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+// Largest bin b of hist[NB] with  sum_{d >= b} hist[d] >= need; sets b and
+// the count strictly above it.  Thread t owns bins [B t, B t + B), B =
+// NB / NT.  All threads of the CTA must call.
+template <int NT, int NB>
+__device__ void cl_select_bin(ClusterSmem<NT> &sm, const uint32_t *hist, uint32_t need, int &bin,
+                              uint32_t &gt)
+{
+    constexpr int kB = NB / NT;
+    constexpr int kNW = NT / 32;
+    static_assert(kB >= 1 && NB % NT == 0, "bins per thread");
+    const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+    uint32_t h[kB];
+    uint32_t local = 0;
+#pragma unroll
+    for (int j = 0; j < kB; ++j) {
+        h[j] = hist[kB * t + j];
+        local += h[j];
+    }
+    uint32_t x = local;                       // inclusive suffix within the warp
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t y = __shfl_down_sync(0xffffffffu, x, off);
+        if (lane + off < 32)
+            x += y;
+    }
+    if (lane == 0)
+        sm.wa[w] = x;
+    __syncthreads();
+    if (w == 0) {
+        const uint32_t tot = lane < kNW ? sm.wa[lane] : 0u;
+        uint32_t y = tot;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const uint32_t z = __shfl_down_sync(0xffffffffu, y, off);
+            if (lane + off < 32)
+                y += z;
+        }
+        if (lane < kNW)
+            sm.wb[lane] = y - tot;
+    }
+    __syncthreads();
+    uint32_t s = sm.wb[w] + (x - local);
+#pragma unroll
+    for (int j = kB - 1; j >= 0; --j) {
+        if (s < need && s + h[j] >= need) {
+            sm.sel_bin = kB * t + j;
+            sm.sel_gt = s;
+        }
+        s += h[j];
+    }
+    __syncthreads();
+    bin = sm.sel_bin;
+    gt = sm.sel_gt;
+}
+
+// Exclusive prefix sum of v over the CTA in thread order; *total = CTA sum.
+template <int NT>
+__device__ __forceinline__ uint32_t cl_excl_scan(ClusterSmem<NT> &sm, uint32_t v, uint32_t *total)
+{
+    constexpr int kNW = NT / 32;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    uint32_t x = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, x, off);
+        if (lane >= off)
+            x += y;
+    }
+    if (lane == 31)
+        sm.wb[w] = x;
+    __syncthreads();
+    if (w == 0) {
+        const uint32_t tot = lane < kNW ? sm.wb[lane] : 0u;
+        uint32_t y = tot;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const uint32_t z = __shfl_up_sync(0xffffffffu, y, off);
+            if (lane >= off)
+                y += z;
+        }
+        if (lane < kNW)
+            sm.wa[lane] = y - tot;
+        if (lane == 31)
+            sm.scan_tot = y;
+    }
+    __syncthreads();
+    const uint32_t base = sm.wa[w];
+    *total = sm.scan_tot;
+    __syncthreads();
+    return base + x - v;
+}
+
+// Adds this CTA's non-zero histogram bins loc[0, NB) into the first CTA's
+// merged histogram `merged` (same offset in its shared memory).
+template <int NT, int NB>
+__device__ __forceinline__ void cl_push(const uint32_t *loc, const uint32_t *merged)
+{
+    const uint32_t m0 = cl_map(merged, 0);
+    for (int i = threadIdx.x; i < NB; i += NT) {
+        const uint32_t c = loc[i];
+        if (c)
+            cl_red_add(m0 + 4u * static_cast<uint32_t>(i), c);
+    }
+}
+
+// In the first CTA: the threshold digit of the merged histogram `hist`,
+// written into every CTA's res[] (the caller then synchronises the cluster).
+template <int NT, int NB>
+__device__ __forceinline__ void cl_broadcast_bin(ClusterSmem<NT> &sm, const uint32_t *hist,
+                                                 uint32_t need, uint32_t ncta)
+{
+    int b;
+    uint32_t gt;
+    cl_select_bin<NT, NB>(sm, hist, need, b, gt);
+    if (threadIdx.x < ncta) {
+        const uint32_t r = cl_map(sm.res, threadIdx.x);
+        cl_st(r, static_cast<uint32_t>(b));
+        cl_st(r + 4u, gt);
+        cl_st(r + 8u, hist[b]);
+    }
+}
+
+template <int NT>
+__global__ void __launch_bounds__(NT, 1024 / NT) topk_cluster_kernel(const TopkParams p)
+{
+    __shared__ ClusterSmem<NT> sm;
+    constexpr int kChunk = kRegPer * NT;
+    const int tid = threadIdx.x;
+    const uint32_t rank = cl_rank(), ncta = cl_nrank();
+    const int64_t row = blockIdx.x / ncta;
+    const int base = static_cast<int>(rank) * kChunk;
+    griddep_wait();
+    griddep_launch_dependents();
+
+    const float *src = p.scores + row * p.in_stride;
+    int V = p.L_row;
+    if (p.valid_len != nullptr) {
+        V = p.valid_len[row];
+        V = V < 0 ? 0 : (V > p.L_row ? p.L_row : V);
+    }
+    const int64_t grp = row / p.rows_per_group;
+    const int64_t orow = grp * p.group_stride + row % p.rows_per_group + p.row_offset;
+    int32_t *oidx = p.idx + orow * p.k;
+    float *oval = p.vals ? p.vals + orow * (p.vals_stride ? p.vals_stride : p.k) : nullptr;
+    const int nsel = p.k < V ? p.k : V;
+    if (rank == 0) {
+        for (int j = nsel + tid; j < p.k; j += NT) {      // padding
+            oidx[j] = p.pad_idx;
+            if (oval)
+                oval[j] = -__int_as_float(0x7f800000);
+        }
+    }
+    if (nsel == V) {
+        // every valid position is selected (no peer is touched: all CTAs of
+        // the cluster take this branch and leave)
+        const int end = min(V, base + kChunk);
+        for (int j = base + tid; j < end; j += NT) {
+            oidx[j] = j;
+            if (oval)
+                oval[j] = src[j];
+        }
+        return;
+    }
+
+    // ---- zero the merged histograms and counters (used in the first CTA)
+    // and this CTA's level-1 histogram; the cluster barrier is completed
+    // only before the first add into a peer
+    if (rank == 0) {
+        for (int i = tid; i < kCB1; i += NT)
+            sm.m1[i] = 0u;
+        for (int i = tid; i < kCB2; i += NT)
+            sm.m2[i] = 0u;
+        for (int i = tid; i < kCB3; i += NT)
+            sm.m3[i] = 0u;
+        if (tid < kClusterMax)
+            sm.tie[tid] = 0u;
+        if (tid == 0) {
+            sm.slot = 0u;
+            sm.ncand = 0u;
+        }
+    }
+    for (int i = tid; i < kCB1; i += NT)
+        sm.loc[i] = 0u;
+    cl_arrive();
+
+    // ---- load: element e of this thread is at position base + 4 (tid + NT (e / 4)) + e % 4
+    uint32_t key[kRegPer];
+    const float *csrc = src + base;
+    if ((reinterpret_cast<uintptr_t>(src) & 15u) == 0 && (p.L_row & 3) == 0) {
+        const float4 *r4 = reinterpret_cast<const float4 *>(csrc);
+        const int lim = p.L_row - base;      // the row's storage past this chunk's start
+        float4 v[kRegPer / 4];
+#pragma unroll
+        for (int i = 0; i < kRegPer / 4; ++i) {
+            const int q = tid + NT * i;
+            v[i] = 4 * q < lim ? __ldg(r4 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int i = 0; i < kRegPer / 4; ++i) {
+            key[4 * i] = float_key(v[i].x);
+            key[4 * i + 1] = float_key(v[i].y);
+            key[4 * i + 2] = float_key(v[i].z);
+            key[4 * i + 3] = float_key(v[i].w);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < kRegPer / 4; ++i) {
+            const int pos = base + 4 * (tid + NT * i);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                key[4 * i + j] = pos + j < V ? float_key(__ldg(src + pos + j)) : 0u;
+        }
+    }
+    const bool full = base + kChunk <= V;
+    auto posof = [&](int e) { return base + 4 * (tid + NT * (e >> 2)) + (e & 3); };
+    auto valid = [&](int e) { return full || posof(e) < V; };
+
+    // ---- level 1
+    __syncthreads();
+#pragma unroll
+    for (int e = 0; e < kRegPer; ++e)
+        if (valid(e))
+            atomicAdd(&sm.loc[key[e] >> 21], 1u);
+    __syncthreads();
+    cl_wait();                                   // the first CTA's zeroing is done
+    cl_push<NT, kCB1>(sm.loc, sm.m1);
+    cl_sync();
+    if (rank == 0)
+        cl_broadcast_bin<NT, kCB1>(sm, sm.m1, static_cast<uint32_t>(nsel), ncta);
+    cl_sync();
+    const uint32_t b1 = sm.res[0];
+    uint32_t need = static_cast<uint32_t>(nsel) - sm.res[1];
+    uint32_t cnt = sm.res[2];
+
+    uint32_t kge;              // keys >= kge are selected ...
+    uint32_t keq = 0u;         // ... and, when tie_quota is set, keys == keq by position
+    bool tie_quota = false;
+    uint32_t quota = 0u;
+    if (cnt == need) {
+        kge = b1 << 21;
+    } else {
+        // ---- level 2: bits [9, 21) of the keys in the level-1 bin
+        for (int i = tid; i < kCB2; i += NT)
+            sm.loc[i] = 0u;
+        __syncthreads();
+#pragma unroll
+        for (int e = 0; e < kRegPer; ++e)
+            if (valid(e) && (key[e] >> 21) == b1)
+                atomicAdd(&sm.loc[(key[e] >> 9) & (kCB2 - 1)], 1u);
+        __syncthreads();
+        cl_push<NT, kCB2>(sm.loc, sm.m2);
+        cl_sync();
+        if (rank == 0)
+            cl_broadcast_bin<NT, kCB2>(sm, sm.m2, need, ncta);
+        cl_sync();
+        const uint32_t t23 = (b1 << 12) | sm.res[0];
+        need -= sm.res[1];
+        cnt = sm.res[2];
+        if (cnt == need) {
+            kge = t23 << 9;
+        } else if (cnt <= static_cast<uint32_t>(kCList)) {
+            // ---- keys above the prefix are written here; those sharing it
+            // are listed in the first CTA, which ranks them
+            uint32_t ns = 0, nc = 0;
+#pragma unroll
+            for (int e = 0; e < kRegPer; ++e) {
+                if (valid(e)) {
+                    const uint32_t pk = key[e] >> 9;
+                    ns += pk > t23 ? 1u : 0u;
+                    nc += pk == t23 ? 1u : 0u;
+                }
+            }
+            uint32_t tot = 0;
+            const uint32_t both = cl_excl_scan(sm, (ns << 16) | nc, &tot);
+            if (tid == 0) {
+                sm.base_s = cl_atom_add(cl_map(&sm.slot, 0), tot >> 16);
+                sm.base_c = cl_atom_add(cl_map(&sm.ncand, 0), tot & 0xFFFFu);
+            }
+            __syncthreads();
+            uint32_t so = sm.base_s + (both >> 16);
+            uint32_t co = sm.base_c + (both & 0xFFFFu);
+            const uint32_t lk = cl_map(sm.loc, 0);
+            const uint32_t lp = lk + 4u * kCList;
+#pragma unroll
+            for (int e = 0; e < kRegPer; ++e) {
+                if (valid(e)) {
+                    const uint32_t pk = key[e] >> 9;
+                    if (pk > t23) {
+                        oidx[so] = posof(e);
+                        if (oval)
+                            oval[so] = key_float(key[e]);
+                        ++so;
+                    } else if (pk == t23) {
+                        cl_st(lk + 4u * co, key[e]);
+                        cl_st(lp + 4u * co, static_cast<uint32_t>(posof(e)));
+                        ++co;
+                    }
+                }
+            }
+            cl_sync();                           // list complete; no peer access after this
+            if (rank == 0) {
+                // rank of each listed key in (key desc, position asc) order
+                const uint32_t first = static_cast<uint32_t>(nsel) - need;
+                const int n = static_cast<int>(cnt);
+                for (int c = tid; c < n; c += NT) {
+                    const uint32_t ck = sm.loc[c];
+                    const uint32_t cp = sm.loc[kCList + c];
+                    uint32_t ahead = 0;
+                    for (int j = 0; j < n; ++j) {
+                        const uint32_t kj = sm.loc[j];
+                        const uint32_t pj = sm.loc[kCList + j];
+                        ahead += (kj > ck || (kj == ck && pj < cp)) ? 1u : 0u;
+                    }
+                    if (ahead < need) {
+                        oidx[first + ahead] = static_cast<int>(cp);
+                        if (oval)
+                            oval[first + ahead] = key_float(ck);
+                    }
+                }
+            }
+            return;
+        } else {
+            // ---- level 3: bits [0, 9) of the keys sharing the prefix
+            for (int i = tid; i < kCB3; i += NT)
+                sm.loc[i] = 0u;
+            __syncthreads();
+#pragma unroll
+            for (int e = 0; e < kRegPer; ++e)
+                if (valid(e) && (key[e] >> 9) == t23)
+                    atomicAdd(&sm.loc[key[e] & (kCB3 - 1)], 1u);
+            __syncthreads();
+            cl_push<NT, kCB3>(sm.loc, sm.m3);
+            cl_sync();
+            if (rank == 0)
+                cl_broadcast_bin<NT, kCB3>(sm, sm.m3, need, ncta);
+            cl_sync();
+            const uint32_t K = (t23 << 9) | sm.res[0];
+            need -= sm.res[1];
+            cnt = sm.res[2];
+            if (cnt == need) {
+                kge = K;
+            } else {
+                // keys equal to K: the `need` lowest positions; CTA c takes
+                // what remains of `need` after the ties of CTAs 0 .. c-1
+                kge = K + 1u;                    // K is a finite score's key: no wrap
+                keq = K;
+                tie_quota = true;
+                uint32_t mine = 0;
+#pragma unroll
+                for (int e = 0; e < kRegPer; ++e)
+                    mine += (valid(e) && key[e] == K) ? 1u : 0u;
+                uint32_t tot = 0;
+                (void)cl_excl_scan(sm, mine, &tot);
+                if (tid == 0)
+                    cl_st(cl_map(&sm.tie[rank], 0), tot);
+                cl_sync();
+                uint32_t before = 0;
+                if (tid == 0) {
+                    const uint32_t t0 = cl_map(sm.tie, 0);
+                    for (uint32_t r = 0; r < rank; ++r)
+                        before += cl_ld(t0 + 4u * r);
+                    sm.base_c = before;
+                }
+                __syncthreads();
+                before = sm.base_c;
+                quota = need > before ? min(need - before, tot) : 0u;
+            }
+        }
+    }
+
+    // ---- write every selected key; output slots from the first CTA's counter
+    uint32_t take_tie = 0u;            // bit e: the tie in element e is taken
+    if (tie_quota && quota > 0u) {
+        uint32_t run = 0;
+#pragma unroll
+        for (int i = 0; i < kRegPer / 4; ++i) {
+            uint32_t c = 0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                c += (valid(4 * i + j) && key[4 * i + j] == keq) ? 1u : 0u;
+            uint32_t tot = 0;
+            uint32_t r = run + cl_excl_scan(sm, c, &tot);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int e = 4 * i + j;
+                if (valid(e) && key[e] == keq) {
+                    if (r < quota)
+                        take_tie |= 1u << e;
+                    ++r;
+                }
+            }
+            run += tot;
+            if (run >= quota)
+                break;              // uniform: every thread sees the same totals
+        }
+    }
+    uint32_t mine = 0;
+#pragma unroll
+    for (int e = 0; e < kRegPer; ++e)
+        mine += (valid(e) && (key[e] >= kge || ((take_tie >> e) & 1u))) ? 1u : 0u;
+    uint32_t tot = 0;
+    uint32_t so = cl_excl_scan(sm, mine, &tot);
+    if (tid == 0)
+        sm.base_s = cl_atom_add(cl_map(&sm.slot, 0), tot);
+    __syncthreads();
+    so += sm.base_s;
+#pragma unroll
+    for (int e = 0; e < kRegPer; ++e) {
+        if (valid(e) && (key[e] >= kge || ((take_tie >> e) & 1u))) {
+            oidx[so] = posof(e);
+            if (oval)
+                oval[so] = key_float(key[e]);
+            ++so;
+        }
+    }
+    cl_sync();                                   // the slot counter is no longer accessed
+}
+
 } // namespace
+
+namespace {
+
+constexpr int kMaxDev = 64;
+constexpr int kClusterNT = 256;
+constexpr int kClusterChunk = kRegPer * kClusterNT;
+
+int current_device()
+{
+    int dev = 0;
+    cudaGetDevice(&dev);
+    return dev < 0 || dev >= kMaxDev ? 0 : dev;
+}
+
+// Largest cluster the cluster path launches on this device: 16 when a
+// cluster of 16 of its CTAs can be resident, else 8 (0 = not yet known).
+int cluster_max(int dev)
+{
+    static std::atomic<int> cmax[kMaxDev];
+    int c = cmax[dev].load(std::memory_order_relaxed);
+    if (c != 0)
+        return c;
+    c = 8;
+    if (cudaFuncSetAttribute(topk_cluster_kernel<kClusterNT>,
+                             cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(kClusterMax);
+        cfg.blockDim = dim3(kClusterNT);
+        cudaLaunchAttribute a[1];
+        a[0].id = cudaLaunchAttributeClusterDimension;
+        a[0].val.clusterDim.x = kClusterMax;
+        a[0].val.clusterDim.y = 1;
+        a[0].val.clusterDim.z = 1;
+        cfg.attrs = a;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, topk_cluster_kernel<kClusterNT>, &cfg) == cudaSuccess &&
+            n > 0)
+            c = kClusterMax;
+    }
+    cudaGetLastError();
+    cmax[dev].store(c, std::memory_order_relaxed);
+    return c;
+}
+
+int sm_count(int dev)
+{
+    static std::atomic<int> sms[kMaxDev];
+    int n = sms[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 1;
+        sms[dev].store(n, std::memory_order_relaxed);
+    }
+    return n;
+}
+
+// CTAs per row of the cluster path for these rows, 0 when they take another
+// path.  The cluster path is taken when all its CTAs fit one per SM: each
+// of its phases then runs on an otherwise idle SM.  With more CTAs than SMs
+// (for example 128 rows of 32K, or 32 of 128K) one CTA per row, or the
+// two-pass path, measured faster: every cluster phase costs a barrier, a
+// release fence and cold instruction fetches.
+int cluster_ctas(const TopkParams &p)
+{
+    if (p.segs > 1 || p.map != nullptr || p.L_row <= kClusterChunk || p.rows <= 0)
+        return 0;
+    const int dev = current_device();
+    const int ncta = (p.L_row + kClusterChunk - 1) / kClusterChunk;
+    if (ncta > cluster_max(dev) || p.rows * ncta > static_cast<int64_t>(sm_count(dev)))
+        return 0;
+    return ncta;
+}
+
+cudaError_t launch_topk_cluster(const TopkParams &p, int ncta, cudaStream_t s)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(p.rows * ncta));
+    cfg.blockDim = dim3(kClusterNT);
+    cfg.stream = s;
+    cudaLaunchAttribute a[2];
+    a[0].id = cudaLaunchAttributeClusterDimension;
+    a[0].val.clusterDim.x = static_cast<unsigned>(ncta);
+    a[0].val.clusterDim.y = 1;
+    a[0].val.clusterDim.z = 1;
+    a[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    a[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = a;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, topk_cluster_kernel<kClusterNT>, p);
+}
+
+} // namespace
+
+bool topk_cluster_path(const TopkParams &p) { return cluster_ctas(p) > 0; }
 
 cudaError_t launch_topk(const TopkParams &p, cudaStream_t s)
 {
     if (p.rows <= 0)
         return cudaSuccess;
-    constexpr int kMaxDev = 64;
     static std::atomic<int> attr_set[kMaxDev];
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= kMaxDev)
-        dev = 0;
+    const int dev = current_device();
+    if (const int ncta = cluster_ctas(p))
+        return launch_topk_cluster(p, ncta, s);
     const int smem = static_cast<int>(sizeof(TopkSmem));
     if (!attr_set[dev].load(std::memory_order_relaxed)) {
         cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);

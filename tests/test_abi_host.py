@@ -123,8 +123,8 @@ def test_topk_workspace_size(L):
 
 def test_hs_workspace_size_and_errors(L):
     ws = L.li_hs_workspace_size(8, 4, 131072, 8192, 2048)
-    # anchor scores, candidate scores, follower scores, anchor top-m in two passes
-    assert ws == 8 * 131072 * 4 + 8 * 8192 * 4 + 8 * 3 * 8192 * 4 + 2 * 8 * 4 * 8192 * 4
+    # anchor scores, every layer's candidate scores, anchor top-m in two passes
+    assert ws == 8 * 131072 * 4 + 8 * 4 * 8192 * 4 + 2 * 8 * 4 * 8192 * 4
     assert L.li_hs_workspace_size(0, 4, 10, 10, 10) == 0
     f = L.li_hs_select
     args = [A, FP8, A, A, FP8, A, A, None, 2, 4, 64, 192, 1000, 256, 64, A, A, A, ws, None]

@@ -380,7 +380,7 @@ def test_hs_matches_oracle(li, orc, dt):
 def test_hs_profiled_equals_hs_and_times_its_stages(li, orc):
     """li_hs_select_profiled does the same work as li_hs_select (identical
     candidates and selections, both checked against the oracle) and records
-    its six events in stream order."""
+    its five events in stream order."""
     w = li_inputs.spec("fp8_128k_hs", B=2, L=40000, m=1024, k=256)
     x = li_inputs.make_workload(w, seed=13)
     c, gi, _ = _hs_check(li, orc, x, 1024, 256, "fp8")
@@ -388,13 +388,13 @@ def test_hs_profiled_equals_hs_and_times_its_stages(li, orc):
     cand = torch.empty(2, 1024, dtype=torch.int32, device=DEV)
     idx = torch.empty(2, 4, 256, dtype=torch.int32, device=DEV)
     ws = torch.empty(li.li_hs_workspace_size(2, 4, 40000, 1024, 256), dtype=torch.uint8, device=DEV)
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
     assert li.li_hs_select_profiled(_dev(x["latent"]), _dev(x["lat_scale"]), qa, qs, _dev(x["w"]),
                                     1024, 256, cand, idx, ws, ev) == 0
     _sync_ok(li)
     np.testing.assert_array_equal(np.sort(cand.cpu().numpy(), axis=-1), np.sort(c, axis=-1))
     np.testing.assert_array_equal(np.sort(idx.cpu().numpy(), axis=-1), np.sort(gi, axis=-1))
-    stages = [ev[i].elapsed_time(ev[i + 1]) for i in range(5)]
+    stages = [ev[i].elapsed_time(ev[i + 1]) for i in range(4)]
     assert all(t >= 0 for t in stages) and sum(stages) > 0
 
 
@@ -537,3 +537,88 @@ def test_topk_unaligned_rows(li, orc):
     assert st == 0 and li.li_device_status() == 0
     oi, _ = orc.topk(s.cpu().double().numpy(), 1000)
     exact_sets_equal(idx.cpu().numpy(), oi)
+
+
+# ------------------------------------------------- top-k: row spread over a cluster
+
+def _cluster_rows(L, g):
+    """Rows built to reach each step of the cluster select: a random row
+    (prefix-sharing list ranked in the first CTA), an exact count at the
+    level-1 and level-2 digits, exact ties at the k-th key (third level and
+    the per-CTA tie quota), one value, and negative / infinite scores."""
+    s = torch.randn(9, L, generator=g) * 3 + 10
+    s[1] = 1.0
+    s[1, torch.randperm(L, generator=g)[:2048]] = 100.0          # level-1 bin holds exactly k
+    s[2] = 1.0
+    s[2, torch.randperm(L, generator=g)[:2048]] = 1.0 + 2.0 ** -12  # same level-1 bin, level 2 exact
+    s[3] = torch.randint(0, 3, (L,), generator=g).float()          # exact ties at the threshold
+    s[4] = 7.0                                                     # one value
+    s[5] = torch.rand(L, generator=g) * 1e-5 + 1.0                 # one narrow binade: level 3
+    s[6, ::3] = float("-inf")
+    s[6, 5] = float("inf")
+    s[7] = -torch.rand(L, generator=g) - 2.0                       # all negative
+    v = s[8].sort(descending=True).values[2047]
+    s[8, torch.randperm(L, generator=g)[:40]] = v                  # a short list of exact ties at k
+    return s
+
+
+@pytest.mark.parametrize("L", [8193, 32768, 50001, 131072])
+def test_topk_cluster_rows_every_branch(li, orc, L):
+    """Few rows longer than 8,192 scores are spread over a thread-block
+    cluster: every branch of its threshold search is bit-exact against the
+    oracle's full sort, with and without valid lengths at CTA borders."""
+    g = torch.Generator().manual_seed(L + 1)
+    s = _cluster_rows(L, g)
+    vl = torch.tensor([L, 8192, 8193, 0, 1, L - 1, 2049, 16383, L], dtype=torch.int32)
+    for k in (1, 100, 2048, 2049, 8192):
+        for v in (None, vl):
+            gi, gv = _topk_gpu(li, s, k, v)
+            oi, ov = orc.topk(s.double().numpy(), k, valid_len=None if v is None else v.numpy())
+            exact_sets_equal(gi, oi)
+            np.testing.assert_array_equal(np.sort(gv, axis=1), np.sort(ov.astype(np.float32), axis=1))
+
+
+def test_topk_cluster_decode_and_anchor_shapes(li, orc):
+    """Decode shapes on scores of the indexer's distribution (non-negative,
+    heavy tail), bit-exact: 128 rows of 32K and 32 rows of 128K (top-2048,
+    more CTAs than SMs: one CTA per row) and the anchor's 8 rows of 128K
+    (top-8192, spread over clusters)."""
+    g = torch.Generator().manual_seed(31)
+    for rows, L, k in ((128, 32768, 2048), (32, 131072, 2048), (8, 131072, 8192)):
+        s = (torch.randn(rows, L, generator=g).clamp_min(0) * 4) ** 2
+        s[:, torch.randperm(L, generator=g)[: L // 100]] *= 16.0
+        gi, gv = _topk_gpu(li, s, k)
+        oi, ov = orc.topk(s.double().numpy(), k)
+        exact_sets_equal(gi, oi)
+        np.testing.assert_array_equal(np.sort(gv, axis=1), np.sort(ov.astype(np.float32), axis=1))
+
+
+def test_topk_many_long_rows_take_the_per_row_paths(li, orc):
+    """With as many long rows as twice the SMs or more, rows are not spread
+    over clusters: one CTA per row (sampled thresholds, the exact fallback
+    and its shared-memory overflow), or the two-pass path with a workspace.
+    Ties across 32K segment borders and valid lengths included."""
+    g = torch.Generator().manual_seed(32)
+    rows, L = 320, 40000
+    s = torch.randn(rows, L, generator=g) * 3 + 10
+    s[1] = torch.randint(0, 7, (L,), generator=g).float()
+    s[2, 30000:36000] = s[2].max() + 1.0
+    s[3] = 1.0 + torch.rand(L, generator=g) * 1e-4             # threshold bin overflows
+    s[4] = 5.0
+    vl = torch.randint(0, L + 1, (rows,), generator=g, dtype=torch.int32)
+    vl[:8] = L
+    sd = s.to(DEV)
+    for k in (1, 2048, 9000):
+        for v in (None, vl):
+            gi, gv = _topk_gpu(li, s, k, v)
+            oi, ov = orc.topk(s.double().numpy(), k, valid_len=None if v is None else v.numpy())
+            exact_sets_equal(gi, oi)
+            np.testing.assert_array_equal(np.sort(gv, axis=1), np.sort(ov.astype(np.float32), axis=1))
+        n = li.li_topk_workspace_size(rows, L, k)
+        if n > 0:
+            ws = torch.empty(n, dtype=torch.uint8, device=DEV)
+            i1 = torch.empty(rows, k, dtype=torch.int32, device=DEV)
+            assert li.li_topk(sd, k, i1, None, ws=ws) == 0
+            _sync_ok(li)
+            oi, _ = orc.topk(s.double().numpy(), k)
+            exact_sets_equal(i1.cpu().numpy(), oi)
