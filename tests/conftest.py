@@ -13,6 +13,26 @@ def pytest_configure(config):
     config.addinivalue_line("markers", "slow: full-size parity case (runs the oracle for many seconds)")
 
 
+def pytest_terminal_summary(terminalreporter):
+    """Score parity totals: how many compared scores the floored rule and the
+    pure relative rule (no floor) each reject."""
+    try:
+        from parity import REPORT
+    except ImportError:
+        return
+    if not REPORT:
+        return
+    n = sum(r[1] for r in REPORT)
+    floored = sum(r[2] for r in REPORT)
+    pure = sum(r[3] for r in REPORT)
+    terminalreporter.write_line(
+        f"score parity: {len(REPORT)} comparisons, {n} scores; outside the floored rule: {floored}; "
+        f"outside the pure relative rule (no floor): {pure}")
+    worst = sorted((r for r in REPORT if r[3]), key=lambda r: -r[3])[:5]
+    for what, cnt, fl, pu in worst:
+        terminalreporter.write_line(f"  {what}: {pu} of {cnt} scores outside the pure relative rule")
+
+
 @pytest.fixture(scope="session")
 def orc():
     import oracle

@@ -26,6 +26,11 @@ import numpy as np
 RTOL = {"f32": 1e-5, "bf16": 2e-2, "fp8": 6e-2}
 FLOOR_FRAC = 0.1
 
+# One entry per assert_scores_close call: (what, scores compared, outside the
+# floored rule, outside the pure relative rule |g - o| <= rtol |o|).  The
+# session summary prints the totals, so the floor's effect stays visible.
+REPORT: list[tuple[str, int, int, int]] = []
+
 
 def _floor(o_row: np.ndarray) -> float:
     v = o_row[np.isfinite(o_row)]
@@ -48,10 +53,13 @@ def assert_scores_close(g, o, rtol: float, what: str = "scores"):
     o = np.asarray(o, dtype=np.float64)
     assert g.shape == o.shape, (g.shape, o.shape)
     _, bad = score_errors(g, o, rtol)
+    pure = int(np.count_nonzero(~(np.abs(g - o) <= rtol * np.abs(o))))
+    REPORT.append((what, int(bad.size), int(bad.sum()), pure))
     if bad.any():
         i = np.argwhere(bad)[0]
         raise AssertionError(
-            f"{what}: {int(bad.sum())} of {bad.size} outside rtol={rtol}; first at {tuple(i)}: "
+            f"{what}: {int(bad.sum())} of {bad.size} outside rtol={rtol} "
+            f"({pure} outside the pure relative rule); first at {tuple(i)}: "
             f"gpu={g[tuple(i)]!r} oracle={o[tuple(i)]!r}")
 
 

@@ -3,14 +3,15 @@ allocate device memory (for example a plugin whose host engine owns all device
 memory, or a decode loop that must not call cudaMalloc).  Its scratch is the
 library's fixed 8 MiB device array; the test checks, through the C ABI, that
 two calls in a row give the same candidates and selections as li_hs_select
-with a caller workspace.  This file is collected last on purpose.
+with a caller workspace, and that both meet the fp64 oracle's hierarchical
+selection under the band rule.  This file is collected last on purpose.
 """
 import numpy as np
 import pytest
 import torch
 
 import li_inputs
-from parity import exact_sets_equal
+from parity import RTOL, assert_topk_row, exact_sets_equal
 
 pytestmark = pytest.mark.gpu
 
@@ -19,12 +20,26 @@ DEV = "cuda:0"
 
 def _inputs(seed):
     w = li_inputs.spec("fp8_128k_hs", B=3, L=20000, m=2048, k=512)
-    x = li_inputs.make_workload(w, seed=seed, device=DEV)
-    return w, x
+    xc = li_inputs.make_workload(w, seed=seed)
+    x = {n: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for n, v in xc.items()}
+    return w, x, xc
 
 
-def test_noalloc_matches_workspace_version_twice(li):
-    w, x = _inputs(7)
+def _check_against_oracle(orc, w, xc, cand, idx):
+    """The candidates are the anchor's top-m and each layer's selection its
+    top-k inside them, against fp64 oracle scores (band rule at fp8's rtol)."""
+    o = orc.score(xc["latent"], xc["lat_scale"], orc.absorb(xc["q"], xc["D"]), xc["w"])[:, 0]
+    c, gi = cand.cpu().numpy(), idx.cpu().numpy()
+    nc = min(w.m, w.L)
+    for b in range(w.B):
+        assert_topk_row(c[b], o[b, 0], w.m, w.L, RTOL["fp8"], f"noalloc cand b{b}")
+        C = set(c[b, :nc].tolist())
+        for l in range(w.G):
+            assert_topk_row(gi[b, l], o[b, l], w.k, w.L, RTOL["fp8"], f"noalloc b{b} l{l}", allowed=C)
+
+
+def test_noalloc_matches_workspace_version_twice(li, orc):
+    w, x, xc = _inputs(7)
     qa, qs = li.absorb_queries(x["q"], x["D"], "fp8")
     ref_c, ref_i = li.hs_select(x["latent"], x["lat_scale"], qa, qs, x["w"], w.m, w.k)
     assert li.li_device_status() == 0
@@ -37,6 +52,7 @@ def test_noalloc_matches_workspace_version_twice(li):
         # identical kernels on identical inputs: the same sets (slot order may differ)
         exact_sets_equal(cand.cpu().numpy(), ref_c.cpu().numpy())
         exact_sets_equal(idx.cpu().numpy(), ref_i.cpu().numpy())
+    _check_against_oracle(orc, w, xc, cand, idx)
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch(li):
