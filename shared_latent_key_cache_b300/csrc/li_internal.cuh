@@ -52,7 +52,11 @@ struct AppendParams {
     int B, dm, r, rR, L;
     float base;            // rotary base
     bool vec;              // dm % 8 == 0 and 16-byte aligned rows: vector loads
+    int kc = 0;            // hidden elements per CTA of a cluster (set by launch_append)
+    int kw = 0;            // hidden elements of P staged in shared memory at a time
+    double theta[128];     // rotary frequencies base^(-2i / rR) (set by launch_append)
 };
+constexpr int kMaxRopePairs = 128;
 cudaError_t launch_append(const AppendParams &p, cudaStream_t s);
 
 // ------------------------------------------------------------- scoring

@@ -88,3 +88,16 @@ def test_append_position_outside_cache_is_skipped_and_reported(li, orc):
     _check_row("fp8", lat[0, 3].cpu(), float(sc[0, 3]), o[0])
     assert (lat[1:].cpu() == 0x5A).all() and (sc[1:].cpu() == -1.0).all()
     assert li.li_device_status() == 0
+
+
+@pytest.mark.parametrize("B,lat_dtype", [(9, "fp8"), (32, "fp8"), (32, "bf16")])
+def test_append_full_hidden_size(li, orc, B, lat_dtype):
+    """The decode size (hidden 7168, r 192, RoPE 64): the hidden dimension is
+    split over a 16-CTA cluster and summed across it; 9 tokens leave a ragged
+    last group of the 4 tokens a cluster takes."""
+    dm, r, rR, L = 7168, 192, 64, 4096
+    pos = [(977 * b) % L for b in range(B)]
+    lat, sc, o, status = _run(li, orc, B, dm, r, rR, L, pos, "bf16", lat_dtype, seed=45 + B)
+    assert status == 0
+    for b in range(B):
+        _check_row(lat_dtype, lat[b, pos[b]].cpu(), None if sc is None else float(sc[b, pos[b]]), o[b])
