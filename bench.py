@@ -32,6 +32,7 @@ sample of the same workload.  Under torchrun each rank runs its own batch
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -59,7 +60,19 @@ def parse():
     ap.add_argument("--no-side", action="store_true", help="skip the HS / native side timings")
     ap.add_argument("--no-configs", action="store_true", help="skip the per-config records")
     ap.add_argument("--cpu-sample-seconds", type=float, default=12.0)
+    ap.add_argument("--shape", default="",
+                    help="override fields of the workload, e.g. T=256,pos0=130816 (a reduced case for "
+                         "profiling; recorded in config.shape_overrides)")
     return ap.parse_args()
+
+
+def shape_overrides(text):
+    """'T=256,pos0=130816' -> {'T': 256, 'pos0': 130816} (integer fields only)."""
+    out = {}
+    for item in filter(None, (t.strip() for t in text.split(","))):
+        key, val = item.split("=", 1)
+        out[key.strip()] = int(val)
+    return out
 
 
 def dist_env():
@@ -267,10 +280,10 @@ def cpu_oracle_rate(w, seed: int, budget_s: float, max_units: int | None = None)
         qpos_all = [w.pos0 + round(i * (w.T - 1) / max(1, cap - 1)) for i in range(cap)]
     while n < cap and (n == 0 or elapsed < budget_s):
         if unit == "sequence":
-            one = li_inputs.spec(w.name, B=1, native=False)
+            one = dataclasses.replace(w, B=1, native=False)
             x = li_inputs.make_workload(one, seed=seed + 1000 + n)
         else:
-            one = li_inputs.spec(w.name, B=1, T=1, native=False, pos0=qpos_all[n])
+            one = dataclasses.replace(w, B=1, T=1, native=False, pos0=qpos_all[n])
             x = li_inputs.make_workload(one, seed=seed + 1000)
         t0 = time.perf_counter()
         qabs = oracle.absorb(x["q"], x["D"])
@@ -561,7 +574,7 @@ def run_ours(a, w):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
 
-    x = li_inputs.make_workload(li_inputs.spec(w.name, native=False), seed=a.seed + rank, device=dev)
+    x = li_inputs.make_workload(dataclasses.replace(w, native=False), seed=a.seed + rank, device=dev)
     stream = torch.cuda.current_stream(dev)
     flush = L2Flush(dev)
     step = Step(li, w, x, dev)
@@ -607,7 +620,7 @@ def run_ours(a, w):
                 "gbs": value, "kernels_us": kb, "roofline": roof, "cpu_baseline": cb,
                 "note": "this record is the contract line itself"}
         if not a.no_side and w.T == 1:
-            sx = li_inputs.make_workload(li_inputs.spec(w.name, native=True), seed=a.seed, device=dev)
+            sx = li_inputs.make_workload(dataclasses.replace(w, native=True), seed=a.seed, device=dev)
             sstep = Step(li, w, sx, dev)
             main.update(side_timings(a, w, sx, sstep, li, stream, flush, dev))
             del sstep, sx
@@ -623,7 +636,8 @@ def run_ours(a, w):
                                                       "bf16": "bf16", "f32": "fp32"}[w.lat_dtype],
                        "step": "absorb + 4-layer group score + per-layer top-k",
                        "l2": "evicted before every step by reading a 256 MiB buffer (no dirty lines left), outside the timed events; inputs also exceed L2",
-                       "parallelism": f"replicas{ws}" if ws > 1 else "single GPU"},
+                       "parallelism": f"replicas{ws}" if ws > 1 else "single GPU",
+                       **({"shape_overrides": shape_overrides(a.shape)} if a.shape else {})},
             "latency_us": ms_per_step * 1e3,
             "tokens_scored_per_s": main["tokens_scored_per_s"],
             "kernels_us": kb,
@@ -750,7 +764,7 @@ def side_timings(a, w, x, step, li, stream, flush, dev):
 def main():
     a = parse()
     import li_inputs
-    w = li_inputs.spec(a.workload)
+    w = li_inputs.spec(a.workload, **shape_overrides(a.shape))
     if a.impl == "reference":
         run_reference(a, w)
     else:
