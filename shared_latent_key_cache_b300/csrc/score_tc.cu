@@ -610,9 +610,9 @@ __global__ void __launch_bounds__(Roles<kGather, kH>::kThreads, 1)
                             sq[j] = sv;
                             bq[j] = p.beta[wrow + j];
                         } else {
-                            // columns 2 and 3 of every 4 take the ReLU as (x + |x|) / 2
-                            // on the FMA pipe (see below): their weight is halved
-                            wq[j] = (j & 3) >= 2 ? 0.5f * (wv * sv) : wv * sv;
+                            // the ReLU is taken as (x + |x|) / 2 (see below): the
+                            // weight is halved
+                            wq[j] = 0.5f * (wv * sv);
                         }
                     }
                     __syncwarp();
@@ -669,17 +669,18 @@ __global__ void __launch_bounds__(Roles<kGather, kH>::kThreads, 1)
 #pragma unroll
                         for (int j = 0; j < 8; ++j) {
                             const float4 ww = w4[j];
-                            // ReLU split between the ALU pipe (fmax, columns 0-1) and
-                            // the FMA pipe (x + |x| = 2 ReLU(x) against a halved
-                            // weight, columns 2-3; both scalings by 2 are exact), so
-                            // that neither pipe carries all of it
+                            // ReLU as x + |x| = 2 ReLU(x) in packed fp32 adds, against
+                            // halved weights (both scalings by 2 are exact, so the sum
+                            // is the same as with max(x, 0) and the full weight); two
+                            // values per instruction instead of a max per value
+                            const float c0 = __uint_as_float(v[4 * j]);
+                            const float c1 = __uint_as_float(v[4 * j + 1]);
                             const float c2 = __uint_as_float(v[4 * j + 2]);
                             const float c3 = __uint_as_float(v[4 * j + 3]);
                             x = __ffma2_rn(make_float2(ww.x, ww.y),
-                                           make_float2(fmaxf(__uint_as_float(v[4 * j]), 0.f),
-                                                       fmaxf(__uint_as_float(v[4 * j + 1]), 0.f)), x);
+                                           __fadd2_rn(make_float2(c0, c1), make_float2(fabsf(c0), fabsf(c1))), x);
                             y = __ffma2_rn(make_float2(ww.z, ww.w),
-                                           make_float2(c2 + fabsf(c2), c3 + fabsf(c3)), y);
+                                           __fadd2_rn(make_float2(c2, c3), make_float2(fabsf(c2), fabsf(c3))), y);
                             if (kH == 16 && (j == 3 || j == 7)) {
                                 finish((col + 4 * j) / 16, (x.x + x.y) + (y.x + y.y));
                                 x = make_float2(0.f, 0.f);
