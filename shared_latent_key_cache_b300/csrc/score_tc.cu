@@ -138,7 +138,10 @@ struct Misc {
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
                                           int *status)
 {
-    const bool ok = mbar_wait(bar, parity, abort, status, kWaitLimitNs);
+    bool ok = mbar_try_wait(bar, parity);
+    if (__all_sync(0xffffffffu, ok))
+        return true;
+    ok = ok || mbar_wait(bar, parity, abort, status, kWaitLimitNs);
     return __all_sync(0xffffffffu, ok);
 }
 
@@ -346,14 +349,19 @@ __global__ void __launch_bounds__(Roles<kGather, kH>::kThreads, 1)
                     break;
                 tc_fence_after();
                 if (lane == 0) {
+                    // descriptors of the stage's and the operand's first K step;
+                    // later steps add their byte offset / 16 to the start-address
+                    // field (shared addresses stay below 2^18, so it cannot carry)
                     const uint32_t a_stage = a_base + static_cast<uint32_t>(stage * c.a_stage_bytes);
+                    const uint64_t ad0 = umma_sdesc(a_stage, kSbo, kSwz);
+                    const uint64_t bd0 = umma_sdesc(b_base, kSbo, kSwz);
                     for (int ch = 0; ch < c.nchunk; ++ch) {
+                        const uint64_t adc = ad0 + static_cast<uint64_t>((ch * c.a_chunk_bytes) >> 4);
+                        const uint64_t bdc = bd0 + static_cast<uint64_t>((ch * c.b_chunk_bytes) >> 4);
 #pragma unroll
                         for (int ks = 0; ks < kStepsPerChunk; ++ks) {
-                            const uint64_t ad = umma_sdesc(
-                                a_stage + static_cast<uint32_t>(ch * c.a_chunk_bytes + ks * 32), kSbo, kSwz);
-                            const uint64_t bd = umma_sdesc(
-                                b_base + static_cast<uint32_t>(ch * c.b_chunk_bytes + ks * 32), kSbo, kSwz);
+                            const uint64_t ad = adc + static_cast<uint64_t>(ks * 2);   // 32 bytes
+                            const uint64_t bd = bdc + static_cast<uint64_t>(ks * 2);
                             const uint32_t accum = (ch | ks) != 0 ? 1u : 0u;
                             if (kFP8)
                                 umma_fp8(d_tmem, ad, bd, idesc, accum);
@@ -542,9 +550,10 @@ __global__ void __launch_bounds__(Roles<kGather, kH>::kThreads, 1)
         const int quarter = warp & 3;               // TMEM lane quarter
         const int c0 = (e >> 2) * kCw;              // first accumulator column
         if (c0 < c.N) {
-            const int ncols = min(kCw, c.N - c0);
+            // at H = 64 every warp owns one whole layer (N is a multiple of 64)
+            const int ncols = kH == 64 ? kCw : min(kCw, c.N - c0);
             const int l0 = c0 / kH;                 // first layer (within the Gs scored)
-            const int nlay = (ncols + kH - 1) / kH;
+            const int nlay = kH == 64 ? 1 : (ncols + kH - 1) / kH;
             const int row = quarter * 32 + lane;
             float *wq = misc->wq + e * kCw;
             float *sq = misc->sq + e * kCw;
@@ -586,6 +595,7 @@ __global__ void __launch_bounds__(Roles<kGather, kH>::kThreads, 1)
             int est = 0;                            // the tile's stage (stage_sc)
             uint32_t est_phase = 0;
             int cur_bt = -1;
+            float *out_row = p.scores;              // this thread's score row start (query row cur_bt)
             while (w.ok()) {
                 int tok2 = 0;
                 if (!stage_sc) {
@@ -617,6 +627,8 @@ __global__ void __launch_bounds__(Roles<kGather, kH>::kThreads, 1)
                     }
                     __syncwarp();
                     cur_bt = w.bt;
+                    out_row = p.scores + (w.bt * (p.Gout ? p.Gout : Gs) + p.gout0 + l0) *
+                                             static_cast<int64_t>(p.L_out) + row;
                 }
                 if (!warp_wait(&bars->tmem_full[acc], acc_phase, abort_flag, p.status))
                     break;
@@ -638,8 +650,7 @@ __global__ void __launch_bounds__(Roles<kGather, kH>::kThreads, 1)
                         est_phase ^= 1u;
                     }
                 }
-                float *out = p.scores + (w.bt * (p.Gout ? p.Gout : Gs) + p.gout0 + l0) *
-                                            static_cast<int64_t>(p.L_out) + pos;
+                float *out = out_row + w.tile * kTileM;
                 const uint32_t tacc = tq + static_cast<uint32_t>(acc * kAccStride);
 
                 auto finish = [&](int lay, float u) {
