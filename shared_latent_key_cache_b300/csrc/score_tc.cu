@@ -416,9 +416,9 @@ __global__ void __launch_bounds__(Roles<kGather, kH>::kThreads, 1)
                 mbar_arrive_expect_tx(&full[stage], static_cast<uint32_t>(c.a_stage_bytes) +
                                                         (c.sc_stage ? kTileM * 4u : 0u));
                 const int b = seq_of(w.bt, p.T);
-                for (int ch = 0; ch < c.nchunk; ++ch)
-                    tma_load_3d_hint(dstA + ch * c.a_chunk_bytes, &tmA, &full[stage],
-                                     ch * kChunkElems, w.tile * kTileM, b, pol);
+                // all K chunks of the tile in one copy (the map's third
+                // dimension is the chunk): [chunk][128 rows][64 elements]
+                tma_load_4d_hint(dstA, &tmA, &full[stage], 0, w.tile * kTileM, 0, b, pol);
                 // the tile's 128 token scales (zero past the cache end)
                 if (c.sc_stage)
                     tma_load_2d(smS + stage * kTileM, &tmS, &full[stage], w.tile * kTileM, b);
@@ -933,15 +933,18 @@ cudaError_t launch_score_tc(const ScoreParams &p, cudaStream_t s)
     const CUtensorMapSwizzle swz = fp8 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
 
     CUtensorMap tmA, tmB, tmS;
-    // latent [B][L][r] as a 3D map {r, L, B}; box {64, 128, 1}
+    // latent [B][L][r] as a 4D map {64, L, r / 64, B} (element k of K chunk
+    // ch of token t at t r + ch 64 + k); box {64, 128, r / 64, 1}: a tile's K
+    // chunks land one after the other, each [128 rows][64 elements]
     {
-        cuuint64_t dims[3] = {static_cast<cuuint64_t>(p.r), static_cast<cuuint64_t>(p.L_lat),
-                              static_cast<cuuint64_t>(p.B)};
-        cuuint64_t strides[2] = {static_cast<cuuint64_t>(p.r) * esz,
+        cuuint64_t dims[4] = {static_cast<cuuint64_t>(kChunkElems), static_cast<cuuint64_t>(p.L_lat),
+                              static_cast<cuuint64_t>(p.r / kChunkElems), static_cast<cuuint64_t>(p.B)};
+        cuuint64_t strides[3] = {static_cast<cuuint64_t>(p.r) * esz,
+                                 static_cast<cuuint64_t>(kChunkElems) * esz,
                                  static_cast<cuuint64_t>(p.r) * esz * p.L_lat};
-        cuuint32_t box[3] = {kChunkElems, kTileM, 1};
-        cuuint32_t estr[3] = {1, 1, 1};
-        if (enc(&tmA, dt, 3, const_cast<void *>(p.latent), dims, strides, box, estr,
+        cuuint32_t box[4] = {kChunkElems, kTileM, static_cast<cuuint32_t>(p.r / kChunkElems), 1};
+        cuuint32_t estr[4] = {1, 1, 1, 1};
+        if (enc(&tmA, dt, 4, const_cast<void *>(p.latent), dims, strides, box, estr,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;

@@ -69,10 +69,10 @@ struct TopkSmem {
 
 __device__ __forceinline__ uint32_t float_key(float x)
 {
-    if (x == 0.f)
-        x = 0.f;                       // fold -0 into +0
-    const uint32_t u = __float_as_uint(x);
-    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    // x + 0 folds -0 into +0 (IEEE round to nearest: -0 + +0 = +0); then
+    // negatives have all bits flipped, non-negatives the sign bit set
+    const uint32_t u = __float_as_uint(x + 0.f);
+    return u ^ (static_cast<uint32_t>(static_cast<int32_t>(u) >> 31) | 0x80000000u);
 }
 
 __device__ __forceinline__ float key_float(uint32_t k)
