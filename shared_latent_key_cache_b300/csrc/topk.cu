@@ -707,7 +707,10 @@ __device__ __forceinline__ uint32_t reg_excl_scan(RegSmem<NT> &sm, uint32_t v, u
     return base + x - v;
 }
 
-template <int NT>
+// kFull: the launch guarantees that every row holds exactly 32 NT valid
+// scores (no valid lengths, no candidate list), so the passes carry no
+// per-element validity test.
+template <int NT, bool kFull>
 __global__ void __launch_bounds__(NT, 1) topk_reg_kernel(const TopkParams p)
 {
     constexpr int kNW = NT / 32;
@@ -788,8 +791,8 @@ __global__ void __launch_bounds__(NT, 1) topk_reg_kernel(const TopkParams p)
                     key[4 * i + j] = pos + j < V ? float_key(__ldg(src + pos + j)) : 0u;
             }
         }
-        const bool full = V == kRegPer * NT;
-        auto valid = [&](int e) { return full || 4 * (tid + NT * (e >> 2)) + (e & 3) < V; };
+        const bool full = kFull || V == kRegPer * NT;
+        auto valid = [&](int e) { return kFull || full || 4 * (tid + NT * (e >> 2)) + (e & 3) < V; };
 
         // ---- key range of the row
         uint32_t lo = 0xFFFFFFFFu, hi = 0u;
@@ -1805,13 +1808,23 @@ cudaError_t launch_topk(const TopkParams &p, cudaStream_t s)
         // Rows indexing a candidate list keep 1024 threads: every selected
         // key's output is a dependent load from the list, fewer per thread.
         const int Lr = p.map != nullptr ? kRegRow : (p.segs > 1 ? p.seg_len : p.L_row);
+        // plain rows exactly as long as the threads' keys, indices only: the
+        // variant without validity tests (for segments, candidate lists or
+        // score outputs it measured slower: more live registers, more spills)
+        const bool rows_full = p.map == nullptr && p.valid_len == nullptr && p.segs <= 1 &&
+                               p.vals == nullptr;
+        const dim3 g(static_cast<unsigned>(grid));
         if (Lr <= 32 * 128)
-            return launch_pdl(topk_reg_kernel<128>, dim3(static_cast<unsigned>(grid)), dim3(128), 0, s, p);
+            return rows_full && Lr == 32 * 128 ? launch_pdl(topk_reg_kernel<128, true>, g, dim3(128), 0, s, p)
+                                               : launch_pdl(topk_reg_kernel<128, false>, g, dim3(128), 0, s, p);
         if (Lr <= 32 * 256)
-            return launch_pdl(topk_reg_kernel<256>, dim3(static_cast<unsigned>(grid)), dim3(256), 0, s, p);
+            return rows_full && Lr == 32 * 256 ? launch_pdl(topk_reg_kernel<256, true>, g, dim3(256), 0, s, p)
+                                               : launch_pdl(topk_reg_kernel<256, false>, g, dim3(256), 0, s, p);
         if (Lr <= 32 * 512)
-            return launch_pdl(topk_reg_kernel<512>, dim3(static_cast<unsigned>(grid)), dim3(512), 0, s, p);
-        return launch_pdl(topk_reg_kernel<1024>, dim3(static_cast<unsigned>(grid)), dim3(1024), 0, s, p);
+            return rows_full && Lr == 32 * 512 ? launch_pdl(topk_reg_kernel<512, true>, g, dim3(512), 0, s, p)
+                                               : launch_pdl(topk_reg_kernel<512, false>, g, dim3(512), 0, s, p);
+        return rows_full && Lr == 32 * 1024 ? launch_pdl(topk_reg_kernel<1024, true>, g, dim3(1024), 0, s, p)
+                                            : launch_pdl(topk_reg_kernel<1024, false>, g, dim3(1024), 0, s, p);
     }
     return launch_pdl(topk_kernel, dim3(static_cast<unsigned>(grid)), dim3(kThreads), static_cast<size_t>(smem), s, p);
 }

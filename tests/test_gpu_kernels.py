@@ -622,3 +622,27 @@ def test_topk_many_long_rows_take_the_per_row_paths(li, orc):
             _sync_ok(li)
             oi, _ = orc.topk(s.double().numpy(), k)
             exact_sets_equal(i1.cpu().numpy(), oi)
+
+
+def test_topk_two_pass_full_segments(li, orc):
+    """Many rows of exactly two 32K segments with a workspace (the two-pass
+    path: more rows than the cluster path takes): ties across the segment
+    border and a one-value row, bit-exact."""
+    g = torch.Generator().manual_seed(33)
+    rows, L = 300, 65536
+    s = torch.randn(rows, L, generator=g) * 3 + 10
+    s[1] = torch.randint(0, 5, (L,), generator=g).float()
+    s[2, 30000:40000] = s[2].max() + 1.0
+    s[3] = 2.5
+    sd = s.to(DEV)
+    for k in (1, 2048, 9000):
+        n = li.li_topk_workspace_size(rows, L, k)
+        assert n > 0
+        ws = torch.empty(n, dtype=torch.uint8, device=DEV)
+        idx = torch.empty(rows, k, dtype=torch.int32, device=DEV)
+        vals = torch.empty(rows, k, dtype=torch.float32, device=DEV)
+        assert li.li_topk(sd, k, idx, vals, ws=ws) == 0
+        _sync_ok(li)
+        oi, ov = orc.topk(s.double().numpy(), k)
+        exact_sets_equal(idx.cpu().numpy(), oi)
+        np.testing.assert_array_equal(np.sort(vals.cpu().numpy(), axis=1), np.sort(ov.astype(np.float32), axis=1))
