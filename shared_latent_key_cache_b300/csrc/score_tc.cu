@@ -71,6 +71,7 @@ constexpr int kMaxDev = 64;
 constexpr int kTmemCols = 512;          // two accumulators of 256 columns
 constexpr int kAccStride = 256;
 constexpr int kConstCap = 1024;         // active epilogue warps x columns per warp
+constexpr int kScRing = 4;              // token-scale slots handed from the MMA warps to the epilogue
 constexpr int kSmemLimit = 227 * 1024;
 
 // Epilogue warps own 64 accumulator columns each (one layer at H = 64), four
@@ -110,6 +111,8 @@ struct TcConfig {
     int cw;             // accumulator columns per epilogue warp
     int nepi;           // epilogue warps with columns
     int sc_stage;       // the latent's per-token scales travel with each tile (TMA into the stage)
+    int sc_ring;        // ... and leave the stage with the tile's MMA warp for a ring slot
+                        // (shallow latent rings), else the epilogue reads them in the stage
     int gdepth;         // gather mode: tiles in flight per copying thread
     int NT;             // tiles per query row
     int64_t U;          // total work units
@@ -118,6 +121,7 @@ struct TcConfig {
 struct __align__(8) Bars {
     uint64_t b_full[2], b_empty[2];
     uint64_t tmem_full[2], tmem_empty[2];
+    uint64_t sc_full[kScRing];              // a tile's token scales are in its ring slot
     uint64_t done;
 };
 
@@ -131,6 +135,9 @@ struct Misc {
     float wq[kConstCap];
     float sq[kConstCap];
     float bq[kConstCap];
+    // token scales of the CTA's tiles ord % kScRing, copied out of the latent
+    // stage by the tile's MMA warp (sc_stage)
+    __align__(16) float scr[kScRing][kTileM];
 };
 
 // The whole (converged) warp waits; the outcome is made warp-uniform, so that
@@ -257,9 +264,9 @@ __global__ void __launch_bounds__(Roles<kGather, kH>::kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < c.stages; ++s) {
             mbar_init(&full[s], kGather ? static_cast<uint32_t>(R::kProdWarps) : 1u);
-            // the MMAs' commit, and each epilogue warp once it has read the
-            // stage's token scales
-            mbar_init(&empty[s], 1u + static_cast<uint32_t>(c.sc_stage ? c.nepi : 0));
+            // the MMAs' commit, and (scales read in the stage) each epilogue
+            // warp once it has read the stage's token scales
+            mbar_init(&empty[s], 1u + static_cast<uint32_t>(c.sc_stage && !c.sc_ring ? c.nepi : 0));
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&bars->b_full[a], 1u);
@@ -267,6 +274,8 @@ __global__ void __launch_bounds__(Roles<kGather, kH>::kThreads, 1)
             mbar_init(&bars->tmem_full[a], 1u);
             mbar_init(&bars->tmem_empty[a], static_cast<uint32_t>(c.nepi));
         }
+        for (int a = 0; a < kScRing; ++a)
+            mbar_init(&bars->sc_full[a], 1u);
         mbar_init(&bars->done, 2u);
         misc->abort = 0;
         mbar_fence_init();
@@ -348,6 +357,19 @@ __global__ void __launch_bounds__(Roles<kGather, kH>::kThreads, 1)
                 if (!warp_wait(&full[stage], phase, abort_flag, p.status))
                     break;
                 tc_fence_after();
+                if (c.sc_ring) {
+                    // The tile's 128 token scales move to its ring slot, so that
+                    // the stage is free again as soon as the MMAs have read it.
+                    // Slot ord % kScRing was last read by the epilogue for tile
+                    // ord - kScRing, which every epilogue warp did before it
+                    // released tile ord - 2's accumulator (waited for above).
+                    const int sl = ord & (kScRing - 1);
+                    reinterpret_cast<float4 *>(misc->scr[sl])[lane] =
+                        reinterpret_cast<const float4 *>(smS + stage * kTileM)[lane];
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(&bars->sc_full[sl]);
+                }
                 if (lane == 0) {
                     // descriptors of the stage's and the operand's first K step;
                     // later steps add their byte offset / 16 to the start-address
@@ -592,7 +614,8 @@ __global__ void __launch_bounds__(Roles<kGather, kH>::kThreads, 1)
             }
             int acc = 0;
             uint32_t acc_phase = 0;
-            int est = 0;                            // the tile's stage (stage_sc)
+            int ord = 0;                            // tile ordinal within the CTA
+            int est = 0;                            // the tile's stage (scales read in the stage)
             uint32_t est_phase = 0;
             int cur_bt = -1;
             float *out_row = p.scores;              // this thread's score row start (query row cur_bt)
@@ -636,7 +659,17 @@ __global__ void __launch_bounds__(Roles<kGather, kH>::kThreads, 1)
                 const int pos = w.tile * kTileM + row;
                 const bool valid = pos < w.Lv;
                 float sc = sc_cur;
-                if (stage_sc) {
+                if (stage_sc && c.sc_ring) {
+                    // the tile's scales, in its ring slot (copied there by its MMA
+                    // warp); the read completes before the accumulator, and with
+                    // it the slot, is released
+                    const int sl = ord & (kScRing - 1);
+                    if (!warp_wait(&bars->sc_full[sl], static_cast<uint32_t>(ord / kScRing) & 1u, abort_flag,
+                                   p.status))
+                        break;
+                    sc = misc->scr[sl][row];
+                    asm volatile("" ::"f"(sc));
+                } else if (stage_sc) {
                     // the stage's copies have landed (their barrier completed before
                     // the MMAs ran); read this token's scale, then give the stage back
                     if (!warp_wait(&full[est], est_phase, abort_flag, p.status))
@@ -754,6 +787,7 @@ __global__ void __launch_bounds__(Roles<kGather, kH>::kThreads, 1)
                 w.next(p, c.NT);
                 sc_cur = sc_next;
                 tok1 = tok2;
+                ++ord;
                 acc ^= 1;
                 if (acc == 0)
                     acc_phase ^= 1u;
@@ -805,6 +839,9 @@ bool make_config(const ScoreParams &p, bool fp8, TcConfig &c, int &smem_bytes)
     if (stages < 2)
         return false;
     c.stages = stages;
+    // a shallow latent ring (the four-layer scan: two 48 KB query buffers
+    // leave 4 stages) is not held up by the epilogue's reading of the scales
+    c.sc_ring = c.sc_stage && stages < 6 ? 1 : 0;
     c.off_a = c.nbuf * c.b_buf_stride;
     c.off_sc = c.off_a + stages * c.a_stage_bytes;
     c.off_bar = c.off_sc + stages * sc_bytes;
