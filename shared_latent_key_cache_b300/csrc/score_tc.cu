@@ -121,7 +121,6 @@ struct TcConfig {
 struct __align__(8) Bars {
     uint64_t b_full[2], b_empty[2];
     uint64_t tmem_full[2], tmem_empty[2];
-    uint64_t sc_full[kScRing];              // a tile's token scales are in its ring slot
     uint64_t done;
 };
 
@@ -271,11 +270,11 @@ __global__ void __launch_bounds__(Roles<kGather, kH>::kThreads, 1)
         for (int a = 0; a < 2; ++a) {
             mbar_init(&bars->b_full[a], 1u);
             mbar_init(&bars->b_empty[a], 2u);      // one commit from each MMA warp
-            mbar_init(&bars->tmem_full[a], 1u);
+            // the MMAs' commit and, with the scale ring, the MMA warp once the
+            // tile's scales are in their slot
+            mbar_init(&bars->tmem_full[a], 1u + static_cast<uint32_t>(c.sc_ring));
             mbar_init(&bars->tmem_empty[a], static_cast<uint32_t>(c.nepi));
         }
-        for (int a = 0; a < kScRing; ++a)
-            mbar_init(&bars->sc_full[a], 1u);
         mbar_init(&bars->done, 2u);
         misc->abort = 0;
         mbar_fence_init();
@@ -363,12 +362,15 @@ __global__ void __launch_bounds__(Roles<kGather, kH>::kThreads, 1)
                     // Slot ord % kScRing was last read by the epilogue for tile
                     // ord - kScRing, which every epilogue warp did before it
                     // released tile ord - 2's accumulator (waited for above).
+                    // The copy is published by an arrival on the accumulator's
+                    // full barrier, whose phase then also waits for the MMAs'
+                    // commit: one wait in the epilogue covers both.
                     const int sl = ord & (kScRing - 1);
                     reinterpret_cast<float4 *>(misc->scr[sl])[lane] =
                         reinterpret_cast<const float4 *>(smS + stage * kTileM)[lane];
                     __syncwarp();
                     if (lane == 0)
-                        mbar_arrive(&bars->sc_full[sl]);
+                        mbar_arrive(&bars->tmem_full[par]);
                 }
                 if (lane == 0) {
                     // descriptors of the stage's and the operand's first K step;
@@ -661,13 +663,10 @@ __global__ void __launch_bounds__(Roles<kGather, kH>::kThreads, 1)
                 float sc = sc_cur;
                 if (stage_sc && c.sc_ring) {
                     // the tile's scales, in its ring slot (copied there by its MMA
-                    // warp); the read completes before the accumulator, and with
-                    // it the slot, is released
-                    const int sl = ord & (kScRing - 1);
-                    if (!warp_wait(&bars->sc_full[sl], static_cast<uint32_t>(ord / kScRing) & 1u, abort_flag,
-                                   p.status))
-                        break;
-                    sc = misc->scr[sl][row];
+                    // warp before the phase of tmem_full just waited for could
+                    // complete); the read completes before the accumulator, and
+                    // with it the slot, is released
+                    sc = misc->scr[ord & (kScRing - 1)][row];
                     asm volatile("" ::"f"(sc));
                 } else if (stage_sc) {
                     // the stage's copies have landed (their barrier completed before
