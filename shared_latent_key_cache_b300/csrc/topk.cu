@@ -44,19 +44,23 @@ namespace li {
 namespace {
 
 constexpr int kThreads = 1024;
-constexpr int kWarps = kThreads / 32;
 constexpr int kBins = 4096;
-constexpr int kCap = 16384;        // (key, position) candidates in shared memory
+constexpr int kCap = 16384;        // (key, position) candidates in shared memory (1024 threads)
 constexpr int kTieCap = 2048;      // ties ranked in shared memory
 constexpr int kSamples = 4096;     // 4 per thread
 constexpr int kMinSampledRow = 8192;
 
+// Shared memory of the long-row kernel with NT threads.  With 512 threads two
+// CTAs share an SM, so the candidate list is half as long.
+template <int NT>
 struct TopkSmem {
+    static constexpr int kNW = NT / 32;
+    static constexpr int kCapN = NT == 1024 ? kCap : kCap / 2;
     uint32_t hist[kBins];
-    uint32_t ckey[kCap];
-    int32_t cpos[kCap];
+    uint32_t ckey[kCapN];
+    int32_t cpos[kCapN];
     int32_t tpos[kTieCap];
-    uint32_t warp_tot[kWarps];
+    uint32_t warp_tot[kNW];
     int emit_cnt;
     int cand_cnt;
     int tie_cnt;
@@ -83,14 +87,14 @@ __device__ __forceinline__ float key_float(uint32_t k)
 
 // Visit every valid element (pos, key) of a row: 16-byte loads when the row
 // is 16-byte aligned, plain coalesced loads otherwise / for the tail.
-template <class F>
+template <int NT, class F>
 __device__ __forceinline__ void for_row(const float *row, int V, F f)
 {
     int head = 0;
     if ((reinterpret_cast<uintptr_t>(row) & 15u) == 0) {
         const int V4 = V & ~3;
         const float4 *r4 = reinterpret_cast<const float4 *>(row);
-        for (int i = threadIdx.x; 4 * i < V4; i += kThreads) {
+        for (int i = threadIdx.x; 4 * i < V4; i += NT) {
             const float4 v = __ldg(r4 + i);
             f(4 * i, float_key(v.x));
             f(4 * i + 1, float_key(v.y));
@@ -99,7 +103,7 @@ __device__ __forceinline__ void for_row(const float *row, int V, F f)
         }
         head = V4;
     }
-    for (int i = head + threadIdx.x; i < V; i += kThreads)
+    for (int i = head + threadIdx.x; i < V; i += NT)
         f(i, float_key(__ldg(row + i)));
 }
 
@@ -121,15 +125,20 @@ __device__ __forceinline__ int reserve(int *counter, bool pred)
 }
 
 // Largest bin b with  sum_{d >= b} hist[d] >= need; returns b and the count
-// strictly above it.  Thread t owns bins [4t, 4t+4).  All threads must call.
-__device__ void select_bin(TopkSmem &sm, uint32_t need, int &bin, uint32_t &gt)
+// strictly above it.  Thread t owns bins [B t, B t + B), B = 4096 / NT.  All
+// threads must call.
+template <int NT>
+__device__ void select_bin(TopkSmem<NT> &sm, uint32_t need, int &bin, uint32_t &gt)
 {
+    constexpr int kB = kBins / NT;
     const int t = threadIdx.x, lane = t & 31, w = t >> 5;
-    uint32_t h[4];
+    uint32_t h[kB];
+    uint32_t local = 0;
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-        h[j] = sm.hist[4 * t + j];
-    const uint32_t local = h[0] + h[1] + h[2] + h[3];
+    for (int j = 0; j < kB; ++j) {
+        h[j] = sm.hist[kB * t + j];
+        local += h[j];
+    }
     uint32_t x = local;                       // inclusive suffix within the warp
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -141,13 +150,13 @@ __device__ void select_bin(TopkSmem &sm, uint32_t need, int &bin, uint32_t &gt)
         sm.warp_tot[w] = x;
     __syncthreads();
     uint32_t above = x - local;
-    for (int w2 = w + 1; w2 < kWarps; ++w2)
+    for (int w2 = w + 1; w2 < NT / 32; ++w2)
         above += sm.warp_tot[w2];
     uint32_t s = above;
 #pragma unroll
-    for (int j = 3; j >= 0; --j) {
+    for (int j = kB - 1; j >= 0; --j) {
         if (s < need && s + h[j] >= need) {
-            sm.sel_bin = 4 * t + j;
+            sm.sel_bin = kB * t + j;
             sm.sel_gt = s;
         }
         s += h[j];
@@ -158,14 +167,16 @@ __device__ void select_bin(TopkSmem &sm, uint32_t need, int &bin, uint32_t &gt)
     __syncthreads();
 }
 
-__device__ __forceinline__ void clear_hist(TopkSmem &sm)
+template <int NT>
+__device__ __forceinline__ void clear_hist(TopkSmem<NT> &sm)
 {
-    for (int i = threadIdx.x; i < kBins; i += kThreads)
+    for (int i = threadIdx.x; i < kBins; i += NT)
         sm.hist[i] = 0u;
 }
 
-// Exclusive prefix sum over the 1024 threads; *total gets the block sum.
-__device__ __forceinline__ uint32_t block_excl_scan(TopkSmem &sm, uint32_t v, uint32_t *total)
+// Exclusive prefix sum over the NT threads; *total gets the block sum.
+template <int NT>
+__device__ __forceinline__ uint32_t block_excl_scan(TopkSmem<NT> &sm, uint32_t v, uint32_t *total)
 {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     uint32_t x = v;
@@ -179,18 +190,19 @@ __device__ __forceinline__ uint32_t block_excl_scan(TopkSmem &sm, uint32_t v, ui
         sm.warp_tot[w] = x;
     __syncthreads();
     if (w == 0) {
-        uint32_t y = sm.warp_tot[lane];
+        uint32_t y = lane < NT / 32 ? sm.warp_tot[lane] : 0u;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
             const uint32_t z = __shfl_up_sync(0xffffffffu, y, off);
             if (lane >= off)
                 y += z;
         }
-        sm.warp_tot[lane] = y;
+        if (lane < NT / 32)
+            sm.warp_tot[lane] = y;
     }
     __syncthreads();
     const uint32_t base = w > 0 ? sm.warp_tot[w - 1] : 0u;
-    *total = sm.warp_tot[kWarps - 1];
+    *total = sm.warp_tot[NT / 32 - 1];
     __syncthreads();
     return base + x - v;
 }
@@ -213,7 +225,8 @@ struct RowOut {
     int k;
 };
 
-__device__ __forceinline__ void emit(TopkSmem &sm, const RowOut &o, bool pred, int pos, uint32_t key)
+template <int NT>
+__device__ __forceinline__ void emit(TopkSmem<NT> &sm, const RowOut &o, bool pred, int pos, uint32_t key)
 {
     const int slot = reserve(&sm.emit_cnt, pred);
     if (pred && slot < o.k) {
@@ -224,14 +237,15 @@ __device__ __forceinline__ void emit(TopkSmem &sm, const RowOut &o, bool pred, i
 }
 
 // In-order pass over the row: emit the `need` lowest positions whose key is K.
-__device__ void tie_pass_global(TopkSmem &sm, const RowOut &o, const float *src, int V, uint32_t K,
+template <int NT>
+__device__ void tie_pass_global(TopkSmem<NT> &sm, const RowOut &o, const float *src, int V, uint32_t K,
                                 uint32_t need)
 {
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     if (tid == 0)
         sm.running = 0;
     __syncthreads();
-    for (int base = 0; base < V; base += kThreads) {
+    for (int base = 0; base < V; base += NT) {
         const int pos = base + tid;
         const bool pred = pos < V && float_key(src[pos]) == K;
         const unsigned m = __ballot_sync(0xffffffffu, pred);
@@ -239,7 +253,7 @@ __device__ void tie_pass_global(TopkSmem &sm, const RowOut &o, const float *src,
             sm.warp_tot[w] = __popc(m);
         __syncthreads();
         uint32_t before = 0, total = 0;
-        for (int w2 = 0; w2 < kWarps; ++w2) {
+        for (int w2 = 0; w2 < NT / 32; ++w2) {
             const uint32_t c = sm.warp_tot[w2];
             before += w2 < w ? c : 0u;
             total += c;
@@ -260,7 +274,8 @@ __device__ void tie_pass_global(TopkSmem &sm, const RowOut &o, const float *src,
 // them.  Returns true when done; false when the ties at the threshold are too
 // many to rank in shared memory (then *Kout / *need_out describe the tie pass
 // the caller runs over the row).
-__device__ bool select_candidates(TopkSmem &sm, const RowOut &o, int n, uint32_t need, uint32_t *Kout,
+template <int NT>
+__device__ bool select_candidates(TopkSmem<NT> &sm, const RowOut &o, int n, uint32_t need, uint32_t *Kout,
                                   uint32_t *need_out)
 {
     const int tid = threadIdx.x;
@@ -269,7 +284,7 @@ __device__ bool select_candidates(TopkSmem &sm, const RowOut &o, int n, uint32_t
     for (int d = 0; d < 3; ++d) {
         clear_hist(sm);
         __syncthreads();
-        for (int i = tid; i < n; i += kThreads) {
+        for (int i = tid; i < n; i += NT) {
             const uint32_t key = sm.ckey[i];
             if ((key & pmask) == prefix)
                 atomicAdd(&sm.hist[digit(key, d)], 1u);
@@ -279,7 +294,7 @@ __device__ bool select_candidates(TopkSmem &sm, const RowOut &o, int n, uint32_t
         uint32_t gt;
         select_bin(sm, need, b, gt);
         last_count = sm.hist[b];
-        for (int i = tid; i < n; i += kThreads) {
+        for (int i = tid; i < n; i += NT) {
             const uint32_t key = sm.ckey[i];
             const bool pred = (key & pmask) == prefix && digit(key, d) > static_cast<uint32_t>(b);
             emit(sm, o, pred, sm.cpos[i], key);
@@ -291,7 +306,7 @@ __device__ bool select_candidates(TopkSmem &sm, const RowOut &o, int n, uint32_t
     }
     const uint32_t K = prefix;           // the k-th largest key; `need` of its copies remain
     if (last_count == need) {
-        for (int i = tid; i < n; i += kThreads)
+        for (int i = tid; i < n; i += NT)
             emit(sm, o, sm.ckey[i] == K, sm.cpos[i], K);
         __syncthreads();
         return true;
@@ -305,7 +320,7 @@ __device__ bool select_candidates(TopkSmem &sm, const RowOut &o, int n, uint32_t
     if (tid == 0)
         sm.tie_cnt = 0;
     __syncthreads();
-    for (int i = tid; i < n; i += kThreads) {
+    for (int i = tid; i < n; i += NT) {
         const bool pred = sm.ckey[i] == K;
         const int slot = reserve(&sm.tie_cnt, pred);
         if (pred)
@@ -313,7 +328,7 @@ __device__ bool select_candidates(TopkSmem &sm, const RowOut &o, int n, uint32_t
     }
     __syncthreads();
     const int nt = sm.tie_cnt;
-    for (int i = tid; i < nt; i += kThreads) {
+    for (int i = tid; i < nt; i += NT) {
         const int pi = sm.tpos[i];
         int rank = 0;
         for (int j = 0; j < nt; ++j)
@@ -324,10 +339,15 @@ __device__ bool select_candidates(TopkSmem &sm, const RowOut &o, int n, uint32_t
     return true;
 }
 
-__global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p)
+// NT = 1024: one CTA per SM (few rows: each row's latency chain is what
+// counts); NT = 512: two CTAs per SM, whose loads, barriers and scans overlap
+// (many rows).
+template <int NT>
+__global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2) topk_kernel(const TopkParams p)
 {
+    constexpr int kCapN = TopkSmem<NT>::kCapN;
     extern __shared__ __align__(16) uint8_t smraw[];
-    TopkSmem &sm = *reinterpret_cast<TopkSmem *>(smraw);
+    TopkSmem<NT> &sm = *reinterpret_cast<TopkSmem<NT> *>(smraw);
     const int tid = threadIdx.x;
     griddep_wait();
     griddep_launch_dependents();
@@ -348,14 +368,14 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p)
         o.k = p.k;
         const int nsel = p.k < V ? p.k : V;
 
-        for (int j = nsel + tid; j < p.k; j += kThreads) {      // padding
+        for (int j = nsel + tid; j < p.k; j += NT) {      // padding
             o.idx[j] = -1;
             if (o.val)
                 o.val[j] = -__int_as_float(0x7f800000);
         }
         if (nsel == V) {
             // everything valid is selected: positions in order
-            for (int j = tid; j < V; j += kThreads) {
+            for (int j = tid; j < V; j += NT) {
                 o.idx[j] = o.map ? o.map[j] : j;
                 if (o.val)
                     o.val[j] = src[j];
@@ -378,7 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p)
         if (V >= kMinSampledRow && rlo_f < 0.3f * kSamples) {
             clear_hist(sm);
             __syncthreads();
-            for (int s2 = tid; s2 < kSamples; s2 += kThreads) {
+            for (int s2 = tid; s2 < kSamples; s2 += NT) {
                 const int lo = static_cast<int>(static_cast<int64_t>(s2) * V / kSamples);
                 const int hi = static_cast<int>(static_cast<int64_t>(s2 + 1) * V / kSamples);
                 const int pos = lo + static_cast<int>(((static_cast<uint32_t>(s2) * 2654435761u) >> 8) %
@@ -397,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p)
                 select_bin(sm, rank, c1, g1);
                 clear_hist(sm);
                 __syncthreads();
-                for (int s2 = tid; s2 < kSamples; s2 += kThreads) {
+                for (int s2 = tid; s2 < kSamples; s2 += NT) {
                     const uint32_t key = sm.ckey[s2];
                     if ((key >> 20) == static_cast<uint32_t>(c1))
                         atomicAdd(&sm.hist[(key >> 8) & 0xFFFu], 1u);
@@ -411,7 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p)
             if (rhi_f >= 1.f) {
                 clear_hist(sm);
                 __syncthreads();
-                for (int s2 = tid; s2 < kSamples; s2 += kThreads)
+                for (int s2 = tid; s2 < kSamples; s2 += NT)
                     atomicAdd(&sm.hist[sm.ckey[s2] >> 20], 1u);
                 __syncthreads();
                 const uint32_t b = sample_bin(static_cast<uint32_t>(rhi_f));
@@ -425,11 +445,11 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p)
             __syncthreads();
             // one pass, 32 scores per thread per 32K chunk held in registers
             const bool al16 = (reinterpret_cast<uintptr_t>(src) & 15u) == 0;
-            for (int base = 0; base < V; base += 32 * kThreads) {
+            for (int base = 0; base < V; base += 32 * NT) {
                 uint32_t key[32];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    const int pos = base + 4 * (tid + kThreads * i);
+                    const int pos = base + 4 * (tid + NT * i);
                     if (al16 && pos + 3 < V) {
                         const float4 v = __ldg(reinterpret_cast<const float4 *>(src + pos));
                         key[4 * i] = float_key(v.x);
@@ -445,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p)
                 uint32_t ns = 0, nb = 0;
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
-                    const int pos = base + 4 * (tid + kThreads * (e / 4)) + (e & 3);
+                    const int pos = base + 4 * (tid + NT * (e / 4)) + (e & 3);
                     const bool ok = pos < V;
                     ns += (ok && key[e] >= T_hi) ? 1u : 0u;
                     nb += (ok && key[e] >= T_lo && key[e] < T_hi) ? 1u : 0u;
@@ -456,7 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p)
                 uint32_t bo = sm.tot_band + (off & 0xFFFFu);
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
-                    const int pos = base + 4 * (tid + kThreads * (e / 4)) + (e & 3);
+                    const int pos = base + 4 * (tid + NT * (e / 4)) + (e & 3);
                     if (pos >= V)
                         continue;
                     if (key[e] >= T_hi) {
@@ -467,7 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p)
                         }
                         ++so;
                     } else if (key[e] >= T_lo) {
-                        if (bo < static_cast<uint32_t>(kCap)) {
+                        if (bo < static_cast<uint32_t>(kCapN)) {
                             sm.ckey[bo] = key[e];
                             sm.cpos[bo] = pos;
                         }
@@ -482,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p)
                 __syncthreads();
             }
             const uint32_t S = sm.tot_sure, Bn = sm.tot_band;
-            have_cands = S < need && S + Bn >= need && Bn <= static_cast<uint32_t>(kCap);
+            have_cands = S < need && S + Bn >= need && Bn <= static_cast<uint32_t>(kCapN);
             if (have_cands) {
                 need -= S;
                 if (tid == 0) {
@@ -506,13 +526,13 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p)
                 sm.cand_cnt = 0;
             }
             __syncthreads();
-            for_row(src, V, [&](int, uint32_t key) { atomicAdd(&sm.hist[key >> 20], 1u); });
+            for_row<NT>(src, V, [&](int, uint32_t key) { atomicAdd(&sm.hist[key >> 20], 1u); });
             __syncthreads();
             uint32_t gt;
             select_bin(sm, need, b1, gt);
-            stored = sm.hist[b1] <= static_cast<uint32_t>(kCap);
+            stored = sm.hist[b1] <= static_cast<uint32_t>(kCapN);
             __syncthreads();
-            for_row(src, V, [&](int pos, uint32_t key) {
+            for_row<NT>(src, V, [&](int pos, uint32_t key) {
                 const uint32_t d1 = key >> 20;
                 emit(sm, o, d1 > static_cast<uint32_t>(b1), pos, key);
                 if (stored) {
@@ -540,7 +560,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p)
             const uint32_t pre1 = static_cast<uint32_t>(b1) << 20;
             clear_hist(sm);
             __syncthreads();
-            for_row(src, V, [&](int, uint32_t key) {
+            for_row<NT>(src, V, [&](int, uint32_t key) {
                 if ((key & 0xFFF00000u) == pre1)
                     atomicAdd(&sm.hist[(key >> 8) & 0xFFFu], 1u);
             });
@@ -552,7 +572,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p)
             const uint32_t pre12 = pre1 | (static_cast<uint32_t>(b2) << 8);
             clear_hist(sm);
             __syncthreads();
-            for_row(src, V, [&](int pos, uint32_t key) {
+            for_row<NT>(src, V, [&](int pos, uint32_t key) {
                 const bool in = (key & 0xFFF00000u) == pre1;
                 const uint32_t d2 = (key >> 8) & 0xFFFu;
                 emit(sm, o, in && d2 > static_cast<uint32_t>(b2), pos, key);
@@ -566,7 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p)
             const uint32_t K = pre12 | static_cast<uint32_t>(b3);
             const bool all_ties = sm.hist[b3] == need;
             __syncthreads();
-            for_row(src, V, [&](int pos, uint32_t key) {
+            for_row<NT>(src, V, [&](int pos, uint32_t key) {
                 const bool in = (key & 0xFFFFFF00u) == pre12;
                 emit(sm, o, in && (key > K || (all_ties && key == K)), pos, key);
             });
@@ -1794,9 +1814,12 @@ cudaError_t launch_topk(const TopkParams &p, cudaStream_t s)
     const int dev = current_device();
     if (const int ncta = cluster_ctas(p))
         return launch_topk_cluster(p, ncta, s);
-    const int smem = static_cast<int>(sizeof(TopkSmem));
     if (!attr_set[dev].load(std::memory_order_relaxed)) {
-        cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        cudaError_t e = cudaFuncSetAttribute(topk_kernel<1024>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(sizeof(TopkSmem<1024>)));
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(topk_kernel<512>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(sizeof(TopkSmem<512>)));
         if (e != cudaSuccess)
             return e;
         attr_set[dev].store(1, std::memory_order_relaxed);
@@ -1826,7 +1849,12 @@ cudaError_t launch_topk(const TopkParams &p, cudaStream_t s)
         return rows_full && Lr == 32 * 1024 ? launch_pdl(topk_reg_kernel<1024, true>, g, dim3(1024), 0, s, p)
                                             : launch_pdl(topk_reg_kernel<1024, false>, g, dim3(1024), 0, s, p);
     }
-    return launch_pdl(topk_kernel, dim3(static_cast<unsigned>(grid)), dim3(kThreads), static_cast<size_t>(smem), s, p);
+    // long rows: with at least two rows per SM, two 512-thread CTAs per SM
+    if (p.rows >= 2 * static_cast<int64_t>(sm_count()))
+        return launch_pdl(topk_kernel<512>, dim3(static_cast<unsigned>(grid)), dim3(512),
+                          sizeof(TopkSmem<512>), s, p);
+    return launch_pdl(topk_kernel<1024>, dim3(static_cast<unsigned>(grid)), dim3(1024), sizeof(TopkSmem<1024>),
+                      s, p);
 }
 
 } // namespace li

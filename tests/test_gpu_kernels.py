@@ -527,6 +527,23 @@ def test_topk_many_long_rows_valid_len(li, orc):
     exact_sets_equal(gi, oi)
 
 
+def test_topk_prefill_rows_two_ctas_per_sm(li, orc):
+    """Causal prefill rows (128K, valid lengths near the causal limit) in a
+    number that puts two 512-thread CTAs on each SM: eight 16K passes per
+    row, a ragged last pass, one row of ties across the threshold."""
+    g = torch.Generator().manual_seed(33)
+    rows, L = 320, 131072
+    s = torch.randn(rows, L, generator=g) * 3 + 20
+    s[7] = torch.randint(0, 5, (L,), generator=g).float()
+    vl = torch.randint(L - 5000, L + 1, (rows,), generator=g, dtype=torch.int32)
+    vl[0] = L
+    vl[1] = 16385
+    gi, gv = _topk_gpu(li, s, 2048, vl)
+    oi, ov = orc.topk(s.double().numpy(), 2048, valid_len=vl.numpy())
+    exact_sets_equal(gi, oi)
+    np.testing.assert_array_equal(np.sort(gv, axis=1), np.sort(ov.astype(np.float32), axis=1))
+
+
 def test_topk_unaligned_rows(li, orc):
     """Row starts that are not 16-byte aligned take the scalar load paths."""
     g = torch.Generator().manual_seed(17)
