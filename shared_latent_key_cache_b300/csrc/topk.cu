@@ -15,7 +15,8 @@
 // A few rows longer than 8,192 scores (all CTAs one per SM) are each spread
 // over a thread-block cluster that merges its histograms in distributed
 // shared memory (the cluster path, further below).
-// Other long rows: one 1024-thread CTA per row, no global scratch memory:
+// Other long rows: one CTA per row, no global scratch memory (1024 threads;
+// 512 threads and two CTAs per SM when there are at least two rows per SM):
 //  1. Sampled thresholds (rows of >= 8192 valid scores selecting at most about
 //     a quarter of them): 4096 stratified samples are histogrammed (12 + 12
 //     key bits) to find two keys whose sample ranks sit five standard
