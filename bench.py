@@ -487,6 +487,65 @@ def config_record(a, name, li, dev, stream, flush, cpu=True):
     return rec
 
 
+class HostPool:
+    """Page-locked host memory for the end-to-end leg: one cudaHostAlloc block
+    (64 MB or more) handing out 2 MB-aligned buffers."""
+
+    ALIGN = 2 << 20
+
+    def __init__(self, nbytes):
+        from cuda.bindings import runtime as rt
+        self.rt = rt
+        self.size = max(64 << 20, -(-nbytes // self.ALIGN) * self.ALIGN)
+        err, self.ptr = rt.cudaHostAlloc(self.size, 0)
+        if err != rt.cudaError_t.cudaSuccess:
+            raise RuntimeError(f"cudaHostAlloc failed: {err}")
+        self.used = 0
+
+    def buffer(self, like):
+        """A HostBuffer holding a copy of the CPU tensor `like`."""
+        n = like.numel() * like.element_size()
+        if self.used + n > self.size:
+            raise RuntimeError("host pool exhausted")
+        b = HostBuffer(self.rt, self.ptr + self.used, like)
+        self.used += -(-n // self.ALIGN) * self.ALIGN
+        return b
+
+    def free(self):
+        self.rt.cudaFreeHost(self.ptr)
+
+
+class HostBuffer:
+    """A CPU tensor view of page-locked pool memory, filled once from `like`
+    by one thread; copies to and from the device are cudaMemcpyAsync calls on
+    the caller's stream.  (Host buffers written by torch's multi-threaded CPU
+    copy were read by every later host-to-device DMA at ~11 GB/s instead of
+    ~50 GB/s, the same bytes written by a single memmove at the full rate:
+    the lines left in many cores' caches slow the device's reads.)"""
+
+    def __init__(self, rt, ptr, like):
+        import ctypes
+        import torch
+        self.rt = rt
+        self.ptr = ptr
+        self.nbytes = like.numel() * like.element_size()
+        raw = (ctypes.c_uint8 * self.nbytes).from_address(self.ptr)
+        self.t = torch.frombuffer(raw, dtype=torch.uint8).view(like.dtype).view(like.shape)
+        src = like.contiguous().view(torch.uint8).numpy()
+        ctypes.memmove(self.ptr, src.ctypes.data, self.nbytes)
+
+    def _copy(self, dst, src, kind, stream):
+        (err,) = self.rt.cudaMemcpyAsync(dst, src, self.nbytes, kind, stream.cuda_stream)
+        if err != self.rt.cudaError_t.cudaSuccess:
+            raise RuntimeError(f"cudaMemcpyAsync failed: {err}")
+
+    def to_device(self, dst, stream):
+        self._copy(dst.data_ptr(), self.ptr, self.rt.cudaMemcpyKind.cudaMemcpyHostToDevice, stream)
+
+    def from_device(self, src, stream):
+        self._copy(self.ptr, src.data_ptr(), self.rt.cudaMemcpyKind.cudaMemcpyDeviceToHost, stream)
+
+
 def e2e_timing(a, w, x, step, li, dev, ws):
     """The same step through the C ABI with host buffers: every step copies its
     queries and head weights from pinned host memory and reads its selections
@@ -495,12 +554,17 @@ def e2e_timing(a, w, x, step, li, dev, ws):
     them; the time is the whole run's, from one event before the first copy to
     the end of the last read-back.  No L2 flush here: every step streams the
     whole latent cache (more than the L2).  Also times a bare pinned copy of
-    the same bytes each way on an idle GPU, the link's own bound."""
+    the same bytes each way on an idle GPU, the link's own bound.  Host
+    buffers are page-locked, from one cudaHostAlloc block, and written once
+    at set-up by one thread."""
     import torch
     stream = torch.cuda.current_stream(dev)
-    q_h = x["q"].cpu().pin_memory()
-    w_h = x["w"].cpu().pin_memory()
     NS = 2
+    idx_bytes = step.idx.numel() * step.idx.element_size()
+    pool = HostPool(x["q"].numel() * x["q"].element_size() + x["w"].numel() * x["w"].element_size() +
+                    NS * idx_bytes + 4 * HostPool.ALIGN)
+    q_h = pool.buffer(x["q"].cpu())
+    w_h = pool.buffer(x["w"].cpu())
     streams = [torch.cuda.Stream(dev) for _ in range(NS)]
     slots = []
     for _ in range(NS):
@@ -508,15 +572,15 @@ def e2e_timing(a, w, x, step, li, dev, ws):
         sx["q"], sx["w"] = torch.empty_like(x["q"]), torch.empty_like(x["w"])
         st = Step(li, w, sx, dev)
         slots.append({"step": st, "x": sx,
-                      "idx_h": torch.empty(st.idx.shape, dtype=torch.int32).pin_memory()})
+                      "idx_h": pool.buffer(torch.empty(st.idx.shape, dtype=torch.int32))})
 
     def e2e_step(i):
         st, sl = streams[i % NS], slots[i % NS]
         with torch.cuda.stream(st):
-            sl["x"]["q"].copy_(q_h, non_blocking=True)
-            sl["x"]["w"].copy_(w_h, non_blocking=True)
+            q_h.to_device(sl["x"]["q"], st)
+            w_h.to_device(sl["x"]["w"], st)
             sl["step"](st)
-            sl["idx_h"].copy_(sl["step"].idx, non_blocking=True)
+            sl["idx_h"].from_device(sl["step"].idx, st)
 
     for i in range(2 * NS):                       # warm the streams
         e2e_step(i)
@@ -537,8 +601,8 @@ def e2e_timing(a, w, x, step, li, dev, ws):
     torch.cuda.synchronize(dev)
     _chk(li, li.li_device_status(stream), "e2e")
     e2e_ms = max_over_ranks(ev_start.elapsed_time(ev_end) / E, ws, dev)
-    h2d = q_h.numel() * q_h.element_size() + w_h.numel() * w_h.element_size()
-    d2h = slots[0]["idx_h"].numel() * slots[0]["idx_h"].element_size()
+    h2d = q_h.nbytes + w_h.nbytes
+    d2h = slots[0]["idx_h"].nbytes
 
     # bare pinned copies of the same sizes, one direction at a time
     def bare(fn, reps=50):
@@ -552,13 +616,16 @@ def e2e_timing(a, w, x, step, li, dev, ws):
         torch.cuda.synchronize(dev)
         return e0.elapsed_time(e1) / reps
     dq, dw = torch.empty_like(x["q"]), torch.empty_like(x["w"])
-    h2d_ms = bare(lambda: (dq.copy_(q_h, non_blocking=True), dw.copy_(w_h, non_blocking=True)))
-    d2h_ms = bare(lambda: slots[0]["idx_h"].copy_(slots[0]["step"].idx, non_blocking=True))
+    h2d_ms = bare(lambda: (q_h.to_device(dq, stream), w_h.to_device(dw, stream)))
+    d2h_ms = bare(lambda: slots[0]["idx_h"].from_device(slots[0]["step"].idx, stream))
+    torch.cuda.synchronize(dev)
+    pool.free()
     return {"ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "steps": E, "streams": NS,
             "link": {"h2d_us": h2d_ms * 1e3, "h2d_gbs": h2d / (h2d_ms * 1e-3) / 1e9,
                      "d2h_us": d2h_ms * 1e3, "d2h_gbs": d2h / (d2h_ms * 1e-3) / 1e9,
-                     "how": "the step's own copies alone on an idle GPU, pinned host memory, mean of 50"}}
+                     "how": "the step's own copies alone on an idle GPU, page-locked host memory "
+                            "(one cudaHostAlloc block), mean of 50"}}
 
 
 def run_ours(a, w):
