@@ -549,9 +549,11 @@ class HostBuffer:
 def e2e_timing(a, w, x, step, li, dev, ws):
     """The same step through the C ABI with host buffers: every step copies its
     queries and head weights from pinned host memory and reads its selections
-    back.  Steps alternate between two streams with their own device buffers,
-    so one step's copies overlap another's kernels, as a serving loop would run
-    them; the time is the whole run's, from one event before the first copy to
+    back.  Steps rotate over three streams with their own device buffers, so
+    one step's copies overlap other steps' kernels, as a serving loop with a
+    few requests in flight would run them (with two, a step's upload waits in
+    its stream for the read-back of the step before it); the time is the
+    whole run's, from one event before the first copy to
     the end of the last read-back.  No L2 flush here: every step streams the
     whole latent cache (more than the L2).  Also times a bare pinned copy of
     the same bytes each way on an idle GPU, the link's own bound.  Host
@@ -559,7 +561,7 @@ def e2e_timing(a, w, x, step, li, dev, ws):
     at set-up by one thread."""
     import torch
     stream = torch.cuda.current_stream(dev)
-    NS = 2
+    NS = 3
     idx_bytes = step.idx.numel() * step.idx.element_size()
     pool = HostPool(x["q"].numel() * x["q"].element_size() + x["w"].numel() * x["w"].element_size() +
                     NS * idx_bytes + 4 * HostPool.ALIGN)
@@ -714,9 +716,9 @@ def run_ours(a, w):
             "wall_s_timed": t_wall,
             "e2e": {"value": whole_job_rate(sb["total"], ws, e2e["ms_per_step"]), "unit": "GB/s",
                     **e2e,
-                    "timing": "whole run of E steps between two events; steps alternate between two "
-                              "streams so copies overlap kernels; no L2 flush (each step streams the "
-                              "whole latent cache)",
+                    "timing": "whole run of E steps between two events; steps rotate over three "
+                              "streams so copies overlap other steps' kernels; no L2 flush (each step "
+                              "streams the whole latent cache)",
                     "resident": "latent cache and decoders (device state across decode steps)"},
             "gpu_launches": launches,
             "roofline": roof,
