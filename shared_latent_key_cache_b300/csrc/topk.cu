@@ -1254,6 +1254,11 @@ __device__ __forceinline__ void cl_arrive()
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 }
 
+__device__ __forceinline__ void cl_arrive_relaxed()
+{
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void cl_wait()
 {
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -1414,8 +1419,10 @@ __device__ __forceinline__ void cl_broadcast_bin(ClusterSmem<NT> &sm, const uint
     }
 }
 
+// At most one CTA per SM runs (the path is taken only when rows x CTAs fit
+// the SMs), so the registers are not capped for more.
 template <int NT>
-__global__ void __launch_bounds__(NT, 1024 / NT) topk_cluster_kernel(const TopkParams p)
+__global__ void __launch_bounds__(NT, 2) topk_cluster_kernel(const TopkParams p)
 {
     __shared__ ClusterSmem<NT> sm;
     constexpr int kChunk = kRegPer * NT;
@@ -1575,23 +1582,26 @@ __global__ void __launch_bounds__(NT, 1024 / NT) topk_cluster_kernel(const TopkP
             uint32_t co = sm.base_c + (both & 0xFFFFu);
             const uint32_t lk = cl_map(sm.loc, 0);
             const uint32_t lp = lk + 4u * kCList;
+            // the list first: the barrier's release then waits for these few
+            // shared-memory stores only, not for the output's global stores
 #pragma unroll
             for (int e = 0; e < kRegPer; ++e) {
-                if (valid(e)) {
-                    const uint32_t pk = key[e] >> 9;
-                    if (pk > t23) {
-                        oidx[so] = posof(e);
-                        if (oval)
-                            oval[so] = key_float(key[e]);
-                        ++so;
-                    } else if (pk == t23) {
-                        cl_st(lk + 4u * co, key[e]);
-                        cl_st(lp + 4u * co, static_cast<uint32_t>(posof(e)));
-                        ++co;
-                    }
+                if (valid(e) && (key[e] >> 9) == t23) {
+                    cl_st(lk + 4u * co, key[e]);
+                    cl_st(lp + 4u * co, static_cast<uint32_t>(posof(e)));
+                    ++co;
                 }
             }
             cl_sync();                           // list complete; no peer access after this
+#pragma unroll
+            for (int e = 0; e < kRegPer; ++e) {
+                if (valid(e) && (key[e] >> 9) > t23) {
+                    oidx[so] = posof(e);
+                    if (oval)
+                        oval[so] = key_float(key[e]);
+                    ++so;
+                }
+            }
             if (rank == 0) {
                 // rank of each listed key in (key desc, position asc) order
                 const uint32_t first = static_cast<uint32_t>(nsel) - need;
@@ -1697,6 +1707,11 @@ __global__ void __launch_bounds__(NT, 1024 / NT) topk_cluster_kernel(const TopkP
     if (tid == 0)
         sm.base_s = cl_atom_add(cl_map(&sm.slot, 0), tot);
     __syncthreads();
+    // the first CTA's slot counter is no longer accessed: a relaxed arrival
+    // now (the atomic has returned), the wait before leaving, so the first
+    // CTA outlives every access to its shared memory while no barrier waits
+    // for the output's global stores
+    cl_arrive_relaxed();
     so += sm.base_s;
 #pragma unroll
     for (int e = 0; e < kRegPer; ++e) {
@@ -1707,7 +1722,7 @@ __global__ void __launch_bounds__(NT, 1024 / NT) topk_cluster_kernel(const TopkP
             ++so;
         }
     }
-    cl_sync();                                   // the slot counter is no longer accessed
+    cl_wait();
 }
 
 } // namespace
