@@ -1203,8 +1203,8 @@ __global__ void __launch_bounds__(NT, 1) topk_reg_kernel(const TopkParams p)
 // merged level and the keys equal to the exact threshold are split between
 // CTAs by position: every position of CTA c precedes those of CTA c + 1.
 
-constexpr int kCB1 = 2048;       // level-1 bins: key bits [21, 32)
-constexpr int kCB2 = 4096;       // level-2 bins: key bits [9, 21)
+constexpr int kCB1 = 8192;       // level-1 bins: key bits [19, 32)
+constexpr int kCB2 = 1024;       // level-2 bins: key bits [9, 19)
 constexpr int kCB3 = 512;        // level-3 bins: key bits [0, 9)
 constexpr int kCList = 256;      // prefix-sharing keys ranked in the first CTA
 constexpr int kClusterMax = 16;
@@ -1212,7 +1212,7 @@ constexpr int kClusterMax = 16;
 template <int NT>
 struct ClusterSmem {
     static constexpr int kNW = NT / 32;
-    uint32_t loc[kCB2];          // this CTA's histogram; first CTA: then the candidate list
+    uint32_t loc[kCB1];          // this CTA's histogram; first CTA: then the candidate list
     uint32_t m1[kCB1];           // merged histograms (first CTA)
     uint32_t m2[kCB2];
     uint32_t m3[kCB3];
@@ -1424,7 +1424,8 @@ __device__ __forceinline__ void cl_broadcast_bin(ClusterSmem<NT> &sm, const uint
 template <int NT>
 __global__ void __launch_bounds__(NT, 2) topk_cluster_kernel(const TopkParams p)
 {
-    __shared__ ClusterSmem<NT> sm;
+    extern __shared__ __align__(16) uint8_t clraw[];
+    ClusterSmem<NT> &sm = *reinterpret_cast<ClusterSmem<NT> *>(clraw);
     constexpr int kChunk = kRegPer * NT;
     const int tid = threadIdx.x;
     const uint32_t rank = cl_rank(), ncta = cl_nrank();
@@ -1521,7 +1522,7 @@ __global__ void __launch_bounds__(NT, 2) topk_cluster_kernel(const TopkParams p)
 #pragma unroll
     for (int e = 0; e < kRegPer; ++e)
         if (valid(e))
-            atomicAdd(&sm.loc[key[e] >> 21], 1u);
+            atomicAdd(&sm.loc[key[e] >> 19], 1u);
     __syncthreads();
     cl_wait();                                   // the first CTA's zeroing is done
     cl_push<NT, kCB1>(sm.loc, sm.m1);
@@ -1538,7 +1539,7 @@ __global__ void __launch_bounds__(NT, 2) topk_cluster_kernel(const TopkParams p)
     bool tie_quota = false;
     uint32_t quota = 0u;
     if (cnt == need) {
-        kge = b1 << 21;
+        kge = b1 << 19;
     } else {
         // ---- level 2: bits [9, 21) of the keys in the level-1 bin
         for (int i = tid; i < kCB2; i += NT)
@@ -1546,7 +1547,7 @@ __global__ void __launch_bounds__(NT, 2) topk_cluster_kernel(const TopkParams p)
         __syncthreads();
 #pragma unroll
         for (int e = 0; e < kRegPer; ++e)
-            if (valid(e) && (key[e] >> 21) == b1)
+            if (valid(e) && (key[e] >> 19) == b1)
                 atomicAdd(&sm.loc[(key[e] >> 9) & (kCB2 - 1)], 1u);
         __syncthreads();
         cl_push<NT, kCB2>(sm.loc, sm.m2);
@@ -1554,7 +1555,7 @@ __global__ void __launch_bounds__(NT, 2) topk_cluster_kernel(const TopkParams p)
         if (rank == 0)
             cl_broadcast_bin<NT, kCB2>(sm, sm.m2, need, ncta);
         cl_sync();
-        const uint32_t t23 = (b1 << 12) | sm.res[0];
+        const uint32_t t23 = (b1 << 10) | sm.res[0];
         need -= sm.res[1];
         cnt = sm.res[2];
         if (cnt == need) {
@@ -1741,7 +1742,8 @@ int current_device()
 }
 
 // Largest cluster the cluster path launches on this device: 16 when a
-// cluster of 16 of its CTAs can be resident, else 8 (0 = not yet known).
+// cluster of 16 of its CTAs can be resident, else 8; -1 when its shared
+// memory cannot be granted (the path is then not taken; 0 = not yet known).
 int cluster_max(int dev)
 {
     static std::atomic<int> cmax[kMaxDev];
@@ -1749,11 +1751,18 @@ int cluster_max(int dev)
     if (c != 0)
         return c;
     c = 8;
+    if (cudaFuncSetAttribute(topk_cluster_kernel<kClusterNT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(sizeof(ClusterSmem<kClusterNT>))) != cudaSuccess) {
+        cudaGetLastError();
+        cmax[dev].store(-1, std::memory_order_relaxed);      // the cluster path is not used
+        return -1;
+    }
     if (cudaFuncSetAttribute(topk_cluster_kernel<kClusterNT>,
                              cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(kClusterMax);
         cfg.blockDim = dim3(kClusterNT);
+        cfg.dynamicSmemBytes = sizeof(ClusterSmem<kClusterNT>);
         cudaLaunchAttribute a[1];
         a[0].id = cudaLaunchAttributeClusterDimension;
         a[0].val.clusterDim.x = kClusterMax;
@@ -1805,6 +1814,7 @@ cudaError_t launch_topk_cluster(const TopkParams &p, int ncta, cudaStream_t s)
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(p.rows * ncta));
     cfg.blockDim = dim3(kClusterNT);
+    cfg.dynamicSmemBytes = sizeof(ClusterSmem<kClusterNT>);
     cfg.stream = s;
     cudaLaunchAttribute a[2];
     a[0].id = cudaLaunchAttributeClusterDimension;
