@@ -67,6 +67,16 @@ __device__ __forceinline__ uint32_t cl_nrank()
     return r;
 }
 
+__device__ __forceinline__ void cluster_arrive_relaxed()
+{
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait()
+{
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void cluster_sync()
 {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
@@ -211,6 +221,10 @@ __device__ void finish_outputs(AppendSmem &sm, const AppendParams &p, int tok0, 
             sm.amax_l[tid] = ld_peer_u32(peer_addr(&sm.amax_s[tid], 0));
         __syncthreads();
     }
+    // This CTA reads no peer from here on (its loads have returned): a
+    // relaxed arrival now and the wait before leaving keep every CTA's shared
+    // memory alive while peers read it, and no release waits for the stores.
+    cluster_arrive_relaxed();
 
     // ---- store into row pos[b] of sequence b
     for (int e = e0 + tid; e < e1; e += kThreads) {
@@ -243,7 +257,7 @@ __device__ void finish_outputs(AppendSmem &sm, const AppendParams &p, int tok0, 
         while (!mbar_try_wait(&sm.bar, drain_parity) && globaltimer_ns() - t0 < kWaitLimitNs) {
         }
     }
-    cluster_sync();                                   // peers no longer read this CTA
+    cluster_wait();                                   // peers no longer read this CTA
 }
 
 // bf16 P with dm % 8 == 0: the CTA's slice of P comes into shared memory by
