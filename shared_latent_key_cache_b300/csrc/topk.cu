@@ -1299,20 +1299,21 @@ __device__ __forceinline__ uint32_t cl_ld(uint32_t addr)
 
 // Largest bin b of hist[NB] with  sum_{d >= b} hist[d] >= need; sets b and
 // the count strictly above it.  Thread t owns bins [B t, B t + B), B =
-// NB / NT.  All threads of the CTA must call.
+// NB / NT (one bin, or none past NB, when NB < NT).  All threads of the CTA
+// must call.
 template <int NT, int NB>
 __device__ void cl_select_bin(ClusterSmem<NT> &sm, const uint32_t *hist, uint32_t need, int &bin,
                               uint32_t &gt)
 {
-    constexpr int kB = NB / NT;
+    constexpr int kB = NB >= NT ? NB / NT : 1;
     constexpr int kNW = NT / 32;
-    static_assert(kB >= 1 && NB % NT == 0, "bins per thread");
+    static_assert(NB >= NT ? NB % NT == 0 : NT % NB == 0, "bins per thread");
     const int t = threadIdx.x, lane = t & 31, w = t >> 5;
     uint32_t h[kB];
     uint32_t local = 0;
 #pragma unroll
     for (int j = 0; j < kB; ++j) {
-        h[j] = hist[kB * t + j];
+        h[j] = kB * t + j < NB ? hist[kB * t + j] : 0u;
         local += h[j];
     }
     uint32_t x = local;                       // inclusive suffix within the warp
@@ -1420,9 +1421,11 @@ __device__ __forceinline__ void cl_broadcast_bin(ClusterSmem<NT> &sm, const uint
 }
 
 // At most one CTA per SM runs (the path is taken only when rows x CTAs fit
-// the SMs), so the registers are not capped for more.
+// the SMs), so the registers are not capped for more.  NT = 256: 8K keys a
+// CTA, up to 16 CTAs a row; NT = 1024: 32K keys a CTA (rows whose 256-thread
+// clusters would not fit the SMs).
 template <int NT>
-__global__ void __launch_bounds__(NT, 2) topk_cluster_kernel(const TopkParams p)
+__global__ void __launch_bounds__(NT, NT >= 1024 ? 1 : 2) topk_cluster_kernel(const TopkParams p)
 {
     extern __shared__ __align__(16) uint8_t clraw[];
     ClusterSmem<NT> &sm = *reinterpret_cast<ClusterSmem<NT> *>(clraw);
@@ -1733,6 +1736,8 @@ namespace {
 constexpr int kMaxDev = 64;
 constexpr int kClusterNT = 256;
 constexpr int kClusterChunk = kRegPer * kClusterNT;
+constexpr int kClusterNTw = 1024;        // the wide cluster kernel
+constexpr int kClusterChunkW = kRegPer * kClusterNTw;
 
 int current_device()
 {
@@ -1792,29 +1797,65 @@ int sm_count(int dev)
     return n;
 }
 
-// CTAs per row of the cluster path for these rows, 0 when they take another
-// path.  The cluster path is taken when all its CTAs fit one per SM: each
-// of its phases then runs on an otherwise idle SM.  With more CTAs than SMs
-// (for example 128 rows of 32K, or 32 of 128K) one CTA per row, or the
-// two-pass path, measured faster: every cluster phase costs a barrier, a
-// release fence and cold instruction fetches.
-int cluster_ctas(const TopkParams &p)
+// The wide cluster kernel's shared memory is granted on this device (set
+// once).
+bool wide_ready(int dev)
 {
-    if (p.segs > 1 || p.map != nullptr || p.L_row <= kClusterChunk || p.rows <= 0)
-        return 0;
-    const int dev = current_device();
-    const int ncta = (p.L_row + kClusterChunk - 1) / kClusterChunk;
-    if (ncta > cluster_max(dev) || p.rows * ncta > static_cast<int64_t>(sm_count(dev)))
-        return 0;
-    return ncta;
+    static std::atomic<int> ok[kMaxDev];
+    int v = ok[dev].load(std::memory_order_relaxed);
+    if (v == 0) {
+        v = cudaFuncSetAttribute(topk_cluster_kernel<kClusterNTw>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(sizeof(ClusterSmem<kClusterNTw>))) == cudaSuccess
+                ? 1
+                : -1;
+        cudaGetLastError();
+        ok[dev].store(v, std::memory_order_relaxed);
+    }
+    return v > 0;
 }
 
+struct ClusterShape {
+    int ncta = 0;          // CTAs per row (0: another path)
+    int nt = 0;            // threads per CTA
+};
+
+// The cluster path's shape for these rows.  It is taken when all its CTAs fit
+// one per SM: each of its phases then runs on an otherwise idle SM.  256
+// threads (8K keys) a CTA when those clusters fit (HS's anchor top-m: 8 rows
+// of 128K -> 128 CTAs), else 1,024 threads (32K keys, clusters of 3-8) when
+// those do (the per-layer top-k of 8 sequences x 4 layers at 128K: 32 rows
+// -> 128 CTAs; 32.8 -> 30.6 us against the two-pass path).  With more CTAs than SMs (for example 128 rows of 32K) one
+// CTA per row measured faster: every cluster phase costs a barrier and cold
+// instruction fetches.
+ClusterShape cluster_shape(const TopkParams &p)
+{
+    ClusterShape c;
+    if (p.segs > 1 || p.map != nullptr || p.L_row <= kClusterChunk || p.rows <= 0)
+        return c;
+    const int dev = current_device();
+    const int64_t sms = sm_count(dev);
+    const int n256 = (p.L_row + kClusterChunk - 1) / kClusterChunk;
+    if (n256 <= cluster_max(dev) && p.rows * n256 <= sms) {
+        c.ncta = n256;
+        c.nt = kClusterNT;
+        return c;
+    }
+    const int nw = (p.L_row + kClusterChunkW - 1) / kClusterChunkW;
+    // rows of at most 64K (two CTAs) measured no faster than the per-row paths
+    if (nw >= 3 && nw <= 8 && p.rows * nw <= sms && wide_ready(dev)) {
+        c.ncta = nw;
+        c.nt = kClusterNTw;
+    }
+    return c;
+}
+
+template <int NT>
 cudaError_t launch_topk_cluster(const TopkParams &p, int ncta, cudaStream_t s)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(p.rows * ncta));
-    cfg.blockDim = dim3(kClusterNT);
-    cfg.dynamicSmemBytes = sizeof(ClusterSmem<kClusterNT>);
+    cfg.blockDim = dim3(NT);
+    cfg.dynamicSmemBytes = sizeof(ClusterSmem<NT>);
     cfg.stream = s;
     cudaLaunchAttribute a[2];
     a[0].id = cudaLaunchAttributeClusterDimension;
@@ -1825,12 +1866,12 @@ cudaError_t launch_topk_cluster(const TopkParams &p, int ncta, cudaStream_t s)
     a[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = a;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, topk_cluster_kernel<kClusterNT>, p);
+    return cudaLaunchKernelEx(&cfg, topk_cluster_kernel<NT>, p);
 }
 
 } // namespace
 
-bool topk_cluster_path(const TopkParams &p) { return cluster_ctas(p) > 0; }
+bool topk_cluster_path(const TopkParams &p) { return cluster_shape(p).ncta > 0; }
 
 cudaError_t launch_topk(const TopkParams &p, cudaStream_t s)
 {
@@ -1838,8 +1879,10 @@ cudaError_t launch_topk(const TopkParams &p, cudaStream_t s)
         return cudaSuccess;
     static std::atomic<int> attr_set[kMaxDev];
     const int dev = current_device();
-    if (const int ncta = cluster_ctas(p))
-        return launch_topk_cluster(p, ncta, s);
+    const ClusterShape cs = cluster_shape(p);
+    if (cs.ncta > 0)
+        return cs.nt == kClusterNT ? launch_topk_cluster<kClusterNT>(p, cs.ncta, s)
+                                   : launch_topk_cluster<kClusterNTw>(p, cs.ncta, s);
     if (!attr_set[dev].load(std::memory_order_relaxed)) {
         cudaError_t e = cudaFuncSetAttribute(topk_kernel<1024>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(sizeof(TopkSmem<1024>)));

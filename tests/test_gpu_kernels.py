@@ -595,11 +595,28 @@ def test_topk_cluster_rows_every_branch(li, orc, L):
             np.testing.assert_array_equal(np.sort(gv, axis=1), np.sort(ov.astype(np.float32), axis=1))
 
 
+@pytest.mark.parametrize("L", [100001, 131072])
+def test_topk_wide_cluster_rows_every_branch(li, orc, L):
+    """More rows than 256-thread clusters fit on the SMs (36 rows), few enough
+    for clusters of 1,024-thread CTAs (32K keys each, 4 per row): every
+    branch of the threshold search, bit-exact, with valid lengths at CTA
+    borders."""
+    g = torch.Generator().manual_seed(L + 7)
+    s = torch.cat([_cluster_rows(L, g) for _ in range(4)])
+    vl = torch.tensor([L, 32768, 32769, 0, 1, L - 1, 2049, 16383, L] * 4, dtype=torch.int32)
+    for k in (1, 2048, 2049, 8192):
+        for v in (None, vl):
+            gi, gv = _topk_gpu(li, s, k, v)
+            oi, ov = orc.topk(s.double().numpy(), k, valid_len=None if v is None else v.numpy())
+            exact_sets_equal(gi, oi)
+            np.testing.assert_array_equal(np.sort(gv, axis=1), np.sort(ov.astype(np.float32), axis=1))
+
+
 def test_topk_cluster_decode_and_anchor_shapes(li, orc):
     """Decode shapes on scores of the indexer's distribution (non-negative,
-    heavy tail), bit-exact: 128 rows of 32K and 32 rows of 128K (top-2048,
-    more CTAs than SMs: one CTA per row) and the anchor's 8 rows of 128K
-    (top-8192, spread over clusters)."""
+    heavy tail), bit-exact: 128 rows of 32K (top-2048, one CTA per row), 32
+    rows of 128K (top-2048, clusters of four 1,024-thread CTAs) and the
+    anchor's 8 rows of 128K (top-8192, clusters of sixteen 256-thread CTAs)."""
     g = torch.Generator().manual_seed(31)
     for rows, L, k in ((128, 32768, 2048), (32, 131072, 2048), (8, 131072, 8192)):
         s = (torch.randn(rows, L, generator=g).clamp_min(0) * 4) ** 2
