@@ -1313,7 +1313,10 @@ __device__ void cl_select_bin(ClusterSmem<NT> &sm, const uint32_t *hist, uint32_
     uint32_t local = 0;
 #pragma unroll
     for (int j = 0; j < kB; ++j) {
-        h[j] = kB * t + j < NB ? hist[kB * t + j] : 0u;
+        if constexpr (NB >= NT)
+            h[j] = hist[kB * t + j];
+        else
+            h[j] = t < NB ? hist[t] : 0u;
         local += h[j];
     }
     uint32_t x = local;                       // inclusive suffix within the warp
