@@ -30,6 +30,15 @@
  *  - Storage types: LI_F32 float, LI_BF16 bfloat16, LI_FP8_E4M3 OCP FP8 E4M3
  *    ("fn") codes with one fp32 scale per row: value = scale * decode(code).
  *    Scales must be >= 0 and finite.
+ *  - Kernels are launched with programmatic stream serialization: a launch
+ *    may be scheduled while the preceding kernel in the stream finishes.  The
+ *    decode scans (li_score_group and li_native_score without q_pos, the HS
+ *    anchor scan) issue the loads of their first cache tiles before waiting
+ *    for that kernel.  A caller kernel that writes the latent / key cache and
+ *    itself triggers programmatic dependents (griddepcontrol.launch_dependents)
+ *    must do so only after those writes and a device-wide fence, as
+ *    li_append_latent does; kernels launched without that trigger are waited
+ *    for in full.
  *  - Calls are reentrant; concurrent calls on different streams are safe.
  *  - The library caches, per device, the device addresses of its own device
  *    variables (the status word; the scratch array of li_hs_select_noalloc),

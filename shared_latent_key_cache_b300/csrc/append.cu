@@ -293,7 +293,6 @@ __global__ void __launch_bounds__(kThreads)
     }
     __syncthreads();
     griddep_wait();
-    griddep_launch_dependents();
 
     const int nbatch = (p.r + 7) / 8;                 // eight latent rows per warp step
     const uint32_t box_bytes = static_cast<uint32_t>(p.r) * kBox * 2u;
@@ -378,6 +377,10 @@ __global__ void __launch_bounds__(kThreads)
         }
     }
     finish_outputs(sm, p, tok0, nt, pending, phase ^ 1u);
+    // the next kernel may start only once this CTA's latent rows are visible
+    // (a scan issues its first latent loads before waiting for this grid)
+    __threadfence();
+    griddep_launch_dependents();
 }
 
 // Any other input types: one thread per latent row, P read from global memory.
@@ -399,7 +402,6 @@ __global__ void __launch_bounds__(kThreads) append_direct_kernel(const AppendPar
         sm.amax_s[tid] = 0u;
     }
     griddep_wait();
-    griddep_launch_dependents();
     float acc[kTok];
 #pragma unroll
     for (int t = 0; t < kTok; ++t)
@@ -440,6 +442,8 @@ __global__ void __launch_bounds__(kThreads) append_direct_kernel(const AppendPar
             sm.part[t][tid] = acc[t];
     }
     finish_outputs(sm, p, tok0, nt, false, 0u);
+    __threadfence();
+    griddep_launch_dependents();
 }
 
 constexpr int kMaxDev = 64;

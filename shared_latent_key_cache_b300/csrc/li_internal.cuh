@@ -126,7 +126,8 @@ constexpr int kTopkRegRow = 32768;
 // kernel may be scheduled while its predecessor in the stream finishes.  The
 // library's kernels execute griddepcontrol.wait (griddep_wait) before their
 // first global memory access, so only their set-up (shared memory, barriers,
-// tensor memory) overlaps the predecessor.
+// tensor memory) overlaps the predecessor; a decode scan's producer also
+// issues its first latent loads (see griddep_wait).
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
                        Args &&...args)

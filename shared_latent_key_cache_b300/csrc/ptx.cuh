@@ -31,7 +31,10 @@ __device__ __forceinline__ uint64_t globaltimer_ns()
 // when launched with programmatic stream serialization) have completed and
 // their memory is visible.  A no-op for a kernel launched without it.  Every
 // kernel of this library executes it in every thread before its first global
-// memory access, so only set-up work overlaps the predecessor.
+// memory access, so only set-up work overlaps the predecessor -- except the
+// TMA producer of a decode scan, which issues the latent loads of its first
+// tiles before it (no kernel of this library writes the latent before
+// letting its dependents start: the append triggers after its stores).
 __device__ __forceinline__ void griddep_wait()
 {
     asm volatile("griddepcontrol.wait;" ::: "memory");

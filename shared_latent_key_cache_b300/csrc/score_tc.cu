@@ -287,7 +287,11 @@ __global__ void __launch_bounds__(Roles<kGather, kH>::kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = misc->tmem_base;
-    griddep_wait();
+    // Each role waits for the preceding kernel (griddep_wait) before its first
+    // global memory access, except the TMA producer of a decode scan, which
+    // first issues the latent loads of its ring's first tiles: the latent cache
+    // is not written by a kernel of this library that lets this one start early
+    // (the append triggers its dependents only after its stores and a fence).
     griddep_launch_dependents();
 
     // Issues the query operand of row bt into buffer (nb % nbuf); returns false
@@ -325,6 +329,7 @@ __global__ void __launch_bounds__(Roles<kGather, kH>::kThreads, 1)
         // with two, one warp's MMAs are queued while the other's execute.
         // Both warps walk every unit (stage ring, query operand buffers), and
         // lane 0 issues the MMAs and commits.
+        griddep_wait();
         const int par = warp == R::kMmaWarp ? 0 : 1;
         const uint32_t idesc = umma_idesc(kFP8, kTileM, c.N);
         const uint32_t a_base = smem_u32(smA);
@@ -425,29 +430,46 @@ __global__ void __launch_bounds__(Roles<kGather, kH>::kThreads, 1)
         int cur_bt = -1;
         int nb = 0;
         int issued = 0;
+        // the latent (and scales) of tile `x` into its stage
+        auto load_tile = [&](const Walk<kGather> &x, int st) {
+            if (lane == 0) {
+                uint8_t *dstA = smA + st * c.a_stage_bytes;
+                mbar_arrive_expect_tx(&full[st], static_cast<uint32_t>(c.a_stage_bytes) +
+                                                     (c.sc_stage ? kTileM * 4u : 0u));
+                const int b = seq_of(x.bt, p.T);
+                // all K chunks of the tile in one copy (the map's third
+                // dimension is the chunk): [chunk][128 rows][64 elements]
+                tma_load_4d_hint(dstA, &tmA, &full[st], 0, x.tile * kTileM, 0, b, pol);
+                // the tile's 128 token scales (zero past the cache end)
+                if (c.sc_stage)
+                    tma_load_2d(smS + st * kTileM, &tmS, &full[st], x.tile * kTileM, b);
+            }
+            __syncwarp();
+        };
         Walk<kGather> w;
-        for (w.init(p, u_begin, u_end, c.NT); w.ok(); w.next(p, c.NT)) {
+        w.init(p, u_begin, u_end, c.NT);
+        // Decode scans (no per-query causal limits to read): the ring's first
+        // tiles before waiting for the preceding kernel; their stages are
+        // still free.
+        int pre = 0;
+        if (p.q_pos == nullptr) {
+            Walk<kGather> x = w;
+            for (; x.ok() && pre < c.stages; x.next(p, c.NT), ++pre)
+                load_tile(x, pre);
+        }
+        griddep_wait();
+        for (; w.ok(); w.next(p, c.NT)) {
             if (w.bt != cur_bt) {
                 if (!load_query_operand(w.bt, nb))
                     break;
                 cur_bt = w.bt;
                 ++nb;
             }
-            if (!warp_wait(&empty[stage], phase ^ 1u, abort_flag, p.status))
-                break;
-            if (lane == 0) {
-                uint8_t *dstA = smA + stage * c.a_stage_bytes;
-                mbar_arrive_expect_tx(&full[stage], static_cast<uint32_t>(c.a_stage_bytes) +
-                                                        (c.sc_stage ? kTileM * 4u : 0u));
-                const int b = seq_of(w.bt, p.T);
-                // all K chunks of the tile in one copy (the map's third
-                // dimension is the chunk): [chunk][128 rows][64 elements]
-                tma_load_4d_hint(dstA, &tmA, &full[stage], 0, w.tile * kTileM, 0, b, pol);
-                // the tile's 128 token scales (zero past the cache end)
-                if (c.sc_stage)
-                    tma_load_2d(smS + stage * kTileM, &tmS, &full[stage], w.tile * kTileM, b);
+            if (issued >= pre) {                 // (the first `pre` were issued before the wait)
+                if (!warp_wait(&empty[stage], phase ^ 1u, abort_flag, p.status))
+                    break;
+                load_tile(w, stage);
             }
-            __syncwarp();
             ++issued;
             if (++stage == c.stages) {
                 stage = 0;
@@ -455,7 +477,11 @@ __global__ void __launch_bounds__(Roles<kGather, kH>::kThreads, 1)
             }
         }
         // Never leave the CTA with copies in flight: wait (bounded) for the
-        // last load issued into each stage and for the last query operands.
+        // last load issued into each stage and for the last query operands
+        // (the tiles issued before the wait count even when the loop stopped
+        // before reaching them).
+        if (issued < pre)
+            issued = pre;
         for (int s2 = 0; s2 < c.stages && s2 < issued; ++s2) {
             const int last = s2 + (issued - 1 - s2) / c.stages * c.stages;   // last tile into s2
             mbar_wait(&full[s2], static_cast<uint32_t>(last / c.stages) & 1u, abort_flag, p.status,
@@ -464,6 +490,7 @@ __global__ void __launch_bounds__(Roles<kGather, kH>::kThreads, 1)
         drain_query_operand(nb);
         __syncwarp();
     } else if (kGather && warp >= R::kProdWarp0 && warp < R::kProdWarp0 + R::kProdWarps) {
+        griddep_wait();
         // ------------------------------- gather producer (2 warps, 64 threads)
         // Thread t copies tile rows t and t + 64 of every unit: the gathered
         // latent rows, as 16-byte cp.async into the swizzled K-major layout TMA
@@ -568,6 +595,7 @@ __global__ void __launch_bounds__(Roles<kGather, kH>::kThreads, 1)
             drain_query_operand(nb);
         __syncwarp();
     } else if (warp >= R::kEpiWarp0) {
+        griddep_wait();
         // ------------------------------------------------------------ epilogue
         constexpr int kCw = EpiShape<kH>::kCols;    // accumulator columns per warp
         const int e = warp - R::kEpiWarp0;

@@ -101,3 +101,27 @@ def test_append_full_hidden_size(li, orc, B, lat_dtype):
     assert status == 0
     for b in range(B):
         _check_row(lat_dtype, lat[b, pos[b]].cpu(), None if sc is None else float(sc[b, pos[b]]), o[b])
+
+
+def test_scan_right_after_append_sees_the_new_rows(li, orc):
+    """A decode scan queued right after an append on the same stream, with no
+    synchronisation between them, scores the appended rows: the scan issues
+    its first cache-tile loads before waiting for the preceding kernel, and
+    the append lets dependents start only after its stores.  4 sequences of
+    4,096 tokens give every CTA a single tile, all loaded before the wait."""
+    from parity import RTOL, assert_scores_close
+    w = li_inputs.spec("fp8_32k_b32", B=4, L=4096, native=False)
+    x = li_inputs.make_workload(w, seed=53)
+    xa, P = li_inputs.make_append_inputs(w.B, 1024, w.r, "bf16", seed=54)
+    pos = torch.tensor([4095, 0, 2000, 128], dtype=torch.int32)
+    lat, lsc = x["latent"].to(DEV), x["lat_scale"].to(DEV)
+    qa, qs = li.absorb_queries(x["q"].to(DEV), x["D"].to(DEV), "fp8")
+    assert li.li_append_latent(xa.to(DEV), P.to(DEV), pos.to(DEV), 64, lat, lsc) == 0
+    s = li.score_group(lat, lsc, qa, qs, x["w"].to(DEV))
+    torch.cuda.synchronize()
+    assert li.li_device_status() == 0
+    lat_h, lsc_h = lat.cpu(), lsc.cpu()
+    for b in range(w.B):                      # the rows did change
+        assert not torch.equal(lat_h[b, pos[b]], x["latent"][b, pos[b]])
+    o = orc.score(lat_h, lsc_h, orc.absorb(x["q"], x["D"]), x["w"])
+    assert_scores_close(s.cpu().numpy(), o, RTOL["fp8"])
